@@ -1,0 +1,227 @@
+// ra_misc.cu — the HBM-bound kernels of the path: the standalone update_out_and_lse merge,
+// the backward preprocess (delta = rowsum(dO * O)) and postprocess (f32 dq -> dq), and the
+// natural <-> shard-major permutations.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ra_internal.h"
+#include "ra_plan.h"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ size_t lse_index(const Plan& P, const SeqDesc& sd, int h, int r, int a) {
+  return sd.lse_off + static_cast<size_t>(h) * P.lse_hstride + static_cast<size_t>(r) * P.shard_stride + a;
+}
+
+unsigned grid_for(long work, long per_block) {
+  long b = (work + per_block - 1) / per_block;
+  if (b > 8192) b = 8192;
+  return static_cast<unsigned>(b < 1 ? 1 : b);
+}
+
+long max_len(const Plan& P) {
+  long m = 0;
+  for (int i = 0; i < P.n_seqs; ++i) m = P.seq[i].L > m ? P.seq[i].L : m;
+  return m;
+}
+
+// ------------------------------------------------------------------ update_out_and_lse
+// lse' = log(e^lse + e^blse); out' = e^(lse-lse') out + e^(blse-lse') bout; -inf identity.
+// One thread per 4 consecutive elements of a (row, head) (VEC = 4) or per element.
+template <typename BT, int VEC>
+__global__ void __launch_bounds__(kThreads)
+    merge_kernel(const __grid_constant__ Plan P, float* __restrict__ out, float* __restrict__ lse,
+                 const BT* __restrict__ bout, const float* __restrict__ blse) {
+  const SeqDesc& sd = P.seq[blockIdx.y];
+  const int L = sd.L, dh = P.head_dim, nv = dh / VEC;
+  const long units = static_cast<long>(plan_ranks(P)) * L * P.hq * nv;
+  for (long u = static_cast<long>(blockIdx.x) * kThreads + threadIdx.x; u < units;
+       u += static_cast<long>(gridDim.x) * kThreads) {
+    const int c = static_cast<int>(u % nv);
+    long x = u / nv;
+    const int h = static_cast<int>(x % P.hq);
+    x /= P.hq;
+    const int a = static_cast<int>(x % L);
+    const int r = P.rank_only >= 0 ? P.rank_only : static_cast<int>(x / L);
+    const size_t li = lse_index(P, sd, h, r, a);
+    const float l1 = lse[li], l2 = blse[li];
+    const float mx = fmaxf(l1, l2);
+    float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
+    if (mx != -INFINITY) {
+      const float e1 = expf(l1 - mx), e2 = expf(l2 - mx);
+      const float s = e1 + e2;
+      lnew = mx + logf(s);
+      w1 = e1 / s;
+      w2 = e2 / s;
+    }
+    const size_t row = static_cast<size_t>(sd.row_off + r * P.shard_stride + a);
+    const size_t e0 = (row * P.hq + h) * dh + static_cast<size_t>(c) * VEC;
+    if (mx != -INFINITY) {
+      if constexpr (VEC == 4) {
+        float4 o = *reinterpret_cast<float4*>(out + e0);
+        float b[4];
+        if constexpr (sizeof(BT) == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(bout + e0);
+          b[0] = t.x; b[1] = t.y; b[2] = t.z; b[3] = t.w;
+        } else {
+          const uint2 t = *reinterpret_cast<const uint2*>(bout + e0);
+          const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
+          const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
+          b[0] = __low2float(p0); b[1] = __high2float(p0);
+          b[2] = __low2float(p1); b[3] = __high2float(p1);
+        }
+        o.x = w1 * o.x + w2 * b[0];
+        o.y = w1 * o.y + w2 * b[1];
+        o.z = w1 * o.z + w2 * b[2];
+        o.w = w1 * o.w + w2 * b[3];
+        *reinterpret_cast<float4*>(out + e0) = o;
+      } else {
+        out[e0] = w1 * out[e0] + w2 * ldf(bout + e0);
+      }
+    }
+    if (c == 0) lse[li] = lnew;
+  }
+}
+
+// ------------------------------------------------------------------ backward preprocess
+// delta[row, h] = sum_d dO[row, h, d] * O[row, h, d]  (f32), one warp per (row, head).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    delta_kernel(const __grid_constant__ Plan P, const T* __restrict__ o, const T* __restrict__ dout,
+                 float* __restrict__ delta) {
+  const SeqDesc& sd = P.seq[blockIdx.y];
+  const int L = sd.L, dh = P.head_dim, lane = threadIdx.x & 31;
+  const long units = static_cast<long>(P.D) * L * P.hq;
+  constexpr int kWarps = kThreads / 32;
+  for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < units;
+       u += static_cast<long>(gridDim.x) * kWarps) {
+    const int h = static_cast<int>(u % P.hq);
+    const int a = static_cast<int>((u / P.hq) % L);
+    const int r = static_cast<int>(u / (static_cast<long>(P.hq) * L));
+    const size_t base = (static_cast<size_t>(sd.row_off + r * P.shard_stride + a) * P.hq + h) * dh;
+    float s = 0.f;
+    for (int d = lane; d < dh; d += 32) s += ldf(o + base + d) * ldf(dout + base + d);
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+    if (lane == 0) delta[lse_index(P, sd, h, r, a)] = s;
+  }
+}
+
+// ------------------------------------------------------------------ backward postprocess
+__global__ void __launch_bounds__(kThreads)
+    dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long n4, float scale) {
+  for (long i = static_cast<long>(blockIdx.x) * kThreads + threadIdx.x; i < n4;
+       i += static_cast<long>(gridDim.x) * kThreads) {
+    const float4 a = acc[i];
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    const __nv_bfloat162 p1 = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&p0);
+    o.y = *reinterpret_cast<const uint32_t*>(&p1);
+    dq[i] = o;
+  }
+}
+
+// ------------------------------------------------------------------ permutations
+// direction 0: natural -> shard-major; 1: shard-major -> natural. One warp per token row.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+    shard_tokens_kernel(const __grid_constant__ Plan P, int direction, const V* __restrict__ src,
+                        V* __restrict__ dst, int nvec) {
+  const SeqDesc& sd = P.seq[blockIdx.y];
+  const int L = sd.L, lane = threadIdx.x & 31;
+  const long units = static_cast<long>(P.D) * L;
+  constexpr int kWarps = kThreads / 32;
+  for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < units;
+       u += static_cast<long>(gridDim.x) * kWarps) {
+    const int a = static_cast<int>(u % L);
+    const int r = static_cast<int>(u / L);
+    const size_t sm = static_cast<size_t>(sd.row_off) + static_cast<size_t>(r) * P.shard_stride + a;
+    const size_t nat = static_cast<size_t>(sd.nat_off) + static_cast<size_t>(layout_pos(P.layout, P.D, L, r, a));
+    const size_t from = direction == 0 ? nat : sm, to = direction == 0 ? sm : nat;
+    for (int c = lane; c < nvec; c += 32) dst[to * nvec + c] = src[from * nvec + c];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    shard_lse_kernel(const __grid_constant__ Plan P, int direction, const float* __restrict__ src,
+                     float* __restrict__ dst) {
+  const SeqDesc& sd = P.seq[blockIdx.y];
+  const int L = sd.L;
+  const long units = static_cast<long>(P.hq) * P.D * L;
+  for (long u = static_cast<long>(blockIdx.x) * kThreads + threadIdx.x; u < units;
+       u += static_cast<long>(gridDim.x) * kThreads) {
+    const int a = static_cast<int>(u % L);
+    const int r = static_cast<int>((u / L) % P.D);
+    const int h = static_cast<int>(u / (static_cast<long>(L) * P.D));
+    const size_t sm = lse_index(P, sd, h, r, a);
+    const size_t nat = static_cast<size_t>(sd.lse_nat_off) + static_cast<size_t>(h) * P.lse_hstride +
+                       static_cast<size_t>(layout_pos(P.layout, P.D, L, r, a));
+    if (direction == 0) dst[sm] = src[nat]; else dst[nat] = src[sm];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const Plan& P, float* out, float* lse, const void* block_out,
+                         int block_f32, const float* block_lse, cudaStream_t st) {
+  const int vec = P.head_dim % 4 == 0 ? 4 : 1;
+  const long work = plan_ranks(P) * max_len(P) * P.hq * (P.head_dim / vec);
+  const dim3 grid(grid_for(work, kThreads), P.n_seqs);
+  if (block_f32) {
+    if (vec == 4) merge_kernel<float, 4><<<grid, kThreads, 0, st>>>(P, out, lse, (const float*)block_out, block_lse);
+    else merge_kernel<float, 1><<<grid, kThreads, 0, st>>>(P, out, lse, (const float*)block_out, block_lse);
+  } else {
+    if (vec == 4) merge_kernel<__nv_bfloat16, 4><<<grid, kThreads, 0, st>>>(P, out, lse, (const __nv_bfloat16*)block_out, block_lse);
+    else merge_kernel<__nv_bfloat16, 1><<<grid, kThreads, 0, st>>>(P, out, lse, (const __nv_bfloat16*)block_out, block_lse);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_delta(const Plan& P, int dtype, const void* out, const void* dout,
+                             float* delta, cudaStream_t st) {
+  const long work = P.D * max_len(P) * P.hq;
+  const dim3 grid(grid_for(work, kThreads / 32), P.n_seqs);
+  if (dtype == RA_F32)
+    delta_kernel<float><<<grid, kThreads, 0, st>>>(P, (const float*)out, (const float*)dout, delta);
+  else
+    delta_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(P, (const __nv_bfloat16*)out, (const __nv_bfloat16*)dout, delta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const Plan& P, const float* dq_acc, void* dq, cudaStream_t st) {
+  const long n4 = static_cast<long>(P.n_rows) * P.hq * P.head_dim / 4;
+  dq_convert_kernel<<<grid_for(n4, kThreads), kThreads, 0, st>>>(
+      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq), n4, P.scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_tokens(const Plan& P, int direction, const void* src, void* dst,
+                                int64_t row_bytes, cudaStream_t st) {
+  const long work = P.D * max_len(P);
+  const dim3 grid(grid_for(work, kThreads / 32), P.n_seqs);
+  const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+  if (row_bytes % 16 == 0 && al % 16 == 0)
+    shard_tokens_kernel<uint4><<<grid, kThreads, 0, st>>>(P, direction, (const uint4*)src, (uint4*)dst, (int)(row_bytes / 16));
+  else if (row_bytes % 4 == 0 && al % 4 == 0)
+    shard_tokens_kernel<uint32_t><<<grid, kThreads, 0, st>>>(P, direction, (const uint32_t*)src, (uint32_t*)dst, (int)(row_bytes / 4));
+  else
+    shard_tokens_kernel<uint8_t><<<grid, kThreads, 0, st>>>(P, direction, (const uint8_t*)src, (uint8_t*)dst, (int)row_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_lse(const Plan& P, int direction, const float* src, float* dst,
+                             cudaStream_t st) {
+  const long work = static_cast<long>(P.hq) * P.D * max_len(P);
+  const dim3 grid(grid_for(work, kThreads), P.n_seqs);
+  shard_lse_kernel<<<grid, kThreads, 0, st>>>(P, direction, src, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

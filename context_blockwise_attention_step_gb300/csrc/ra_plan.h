@@ -1,0 +1,122 @@
+// ra_plan.h — the launch plan every kernel receives by value: problem constants, the
+// per-sequence table (the varlen tile scheduler's input) and the work-item decoding.
+//
+// Varlen mode packs several sequences (cu_seqlens); batch mode is the special case of B
+// equal sequences. Each sequence i is split into D pieces of L_i = len_i/D local tokens;
+// the shard-major row of local token a of rank r is row_off_i + r*shard_stride + a and its
+// natural row is nat_off_i + layout_pos(r, a). The host sorts the table by length
+// (longest first) so that a persistent grid starts with the biggest work.
+#pragma once
+#include <stdint.h>
+
+#include "ra_layout.h"
+#include "../../include/ringattn.h"
+
+namespace ra {
+
+constexpr int kFwdBlockRows = 256;  // query rows per forward work item (two 128-row tiles)
+constexpr int kKvTileRows = 128;    // K/V rows per tile (and per backward work item)
+constexpr int kQTileRows = 128;
+
+struct SeqDesc {
+  int32_t row_off;      // shard-major row of (rank 0, local token 0)
+  int32_t nat_off;      // natural row of the sequence's first token
+  int32_t L;            // local length len_i / D
+  int32_t lse_off;      // shard-major lse index of (rank 0, local 0), head 0
+  int32_t lse_nat_off;  // natural lse index of the sequence's first token, head 0
+  int32_t item_start;   // first work item of this sequence in the launched kernel
+};
+
+struct Plan {
+  int32_t layout, causal, D;
+  int32_t hq, hkv, group, head_dim;
+  int32_t shard_stride;  // rows between rank r and rank r+1 of one sequence piece
+  int32_t lse_hstride;   // lse elements between heads
+  int32_t n_rows;        // rows of the token axis (B*S or T)
+  int32_t n_seqs, n_items;
+  int32_t step_begin, step_end;  // ring steps covered by a forward launch
+  int32_t rank_only;             // >= 0: only this rank's query rows (block mode)
+  int32_t out_f32;               // forward output stored as float32 (else problem dtype)
+  float scale, scale_log2;
+  uint64_t timeout_ns;
+  SeqDesc seq[RA_MAX_SEQS];
+};
+
+RA_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+RA_HD int plan_ranks(const Plan& P) { return P.rank_only >= 0 ? 1 : P.D; }
+
+// Forward items of one sequence: one per (256-row query block, rank, query head).
+RA_HD int fwd_items_of(const Plan& P, int L) {
+  return ceil_div(L, kFwdBlockRows) * plan_ranks(P) * P.hq;
+}
+// Backward items of one sequence: one per (128-row K/V tile, rank, K/V head).
+RA_HD int bwd_items_of(const Plan& P, int L) {
+  return ceil_div(L, kKvTileRows) * P.D * P.hkv;
+}
+
+RA_HD int find_seq(const Plan& P, int w) {
+  int lo = 0, hi = P.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.seq[mid].item_start <= w) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct FwdItem { int seq, h, r, blk; };
+struct BwdItem { int seq, hk, j, kt; };
+
+// Forward decode: the last query block first (for causal layouts it sees the most keys),
+// ranks next, query heads innermost (the heads of a GQA group then read the same K/V
+// tiles at about the same time, from L2).
+RA_HD FwdItem decode_fwd(const Plan& P, int w) {
+  FwdItem it;
+  it.seq = find_seq(P, w);
+  const SeqDesc& s = P.seq[it.seq];
+  int x = w - s.item_start;
+  it.h = x % P.hq;
+  x /= P.hq;
+  const int nr = plan_ranks(P);
+  it.r = P.rank_only >= 0 ? P.rank_only : x % nr;
+  x /= nr;
+  it.blk = ceil_div(s.L, kFwdBlockRows) - 1 - x;
+  return it;
+}
+
+// Backward decode: K/V tiles in increasing order (early keys are seen by the most
+// queries), shards next, K/V heads innermost.
+RA_HD BwdItem decode_bwd(const Plan& P, int w) {
+  BwdItem it;
+  it.seq = find_seq(P, w);
+  const SeqDesc& s = P.seq[it.seq];
+  int x = w - s.item_start;
+  it.hk = x % P.hkv;
+  x /= P.hkv;
+  it.j = x % P.D;
+  it.kt = x / P.D;
+  return it;
+}
+
+// Number of K/V tiles of shard j that a query block of rank r whose last valid local row
+// is a_last must visit (a prefix of the shard's tiles).
+RA_HD int kv_tiles_for(const Plan& P, int L, int r, int j, int a_last) {
+  if (!P.causal) return ceil_div(L, kKvTileRows);
+  const int lim = key_limit(P.layout, P.D, L, j, layout_pos(P.layout, P.D, L, r, a_last));
+  return lim < 0 ? 0 : lim / kKvTileRows + 1;
+}
+
+// Number of keys of K/V tile b (shard j) that the query at local row a of rank r sees.
+RA_HD int row_key_count(const Plan& P, int L, int r, int a, int j, int b) {
+  if (a >= L) return 0;
+  const int lim = P.causal ? key_limit(P.layout, P.D, L, j, layout_pos(P.layout, P.D, L, r, a))
+                           : L - 1;
+  int c = lim + 1 - b * kKvTileRows;
+  return c < 0 ? 0 : (c > kKvTileRows ? kKvTileRows : c);
+}
+
+// Rank that holds K/V shard j at ring step s, and the shard rank r holds at step s.
+RA_HD int rank_at_step(int D, int j, int s) { return (j + s) % D; }
+RA_HD int shard_at_step(int D, int r, int s) { return ((r - s) % D + D) % D; }
+
+}  // namespace ra
