@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Ring attention fwd+bwd throughput on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch of synthetic input: the fused ring
+forward (all D steps, online-softmax merge, finalise) and the ring backward (preprocess,
+K/V-tile kernel, postprocess), on shard-major inputs resident in HBM. ``value`` is
+algorithmic fwd+bwd TFLOP/s (causal pairs only, backward = 2.5x forward) on the
+long-context workload: 131072 tokens, 32 query / 8 K/V heads, head_dim 128, D = 16,
+zigzag, causal, bf16.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead (a bounded
+sample of query rows per step). With ``--gpus N`` under torchrun each rank runs its own
+replica of the workload (the path has no cross-GPU exchange); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "ring-attn fwd+bwd TFLOP/s (causal bf16, 1×GB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, with the sha256 prefix
+# of the kernel source they were taken on (a changed kernel reports null until re-measured).
+TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.LONG128K.name, choices=sorted(W.NAMED))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of one oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def fwd_bwd_flops(w: W.Workload) -> tuple[float, float]:
+    f = w.fwd_flops()
+    return f, 2.5 * f
+
+
+# ------------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(w: W.Workload, target_s: float, inputs=None):
+    """Time the float64 oracle (forward + backward) on the last R query rows of the longest
+    sequence, every head; R grows until one sample takes about ``target_s`` / 4 or more.
+
+    Returns (TFLOP/s, seconds, description)."""
+    from oracle import attention as A
+
+    if inputs is None:
+        q, k, v = W.make_qkv(w)
+        do = W.make_dout(w)
+    else:
+        q, k, v, do = inputs
+    pk = lambda x: x.reshape(-1, x.shape[-2], x.shape[-1])
+    q, k, v, do = pk(q), pk(k), pk(v), pk(do)
+    i = int(np.argmax(w.lengths))
+    cu = w.cu_seqlens
+    s0, s1 = int(cu[i]), int(cu[i + 1])
+    qs, ks, vs, dos = q[s0:s1], k[s0:s1], v[s0:s1], do[s0:s1]
+    cu1 = np.array([0, s1 - s0])
+
+    def run(nrows):
+        rows = np.arange(s1 - s0 - nrows, s1 - s0)
+        t0 = time.perf_counter()
+        A.attention_fwd(qs, ks, vs, cu1, w.causal, rows=rows)
+        A.attention_bwd(qs, ks, vs, dos, cu1, w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        pairs = float(sum((r + 1) if w.causal else (s1 - s0) for r in rows)) * w.hq
+        return dt, 3.5 * 4.0 * w.head_dim * pairs
+
+    n = 4
+    dt, fl = run(n)
+    while dt < target_s / 4 and n < (s1 - s0):
+        n = min(s1 - s0, max(n * 2, int(n * target_s / max(dt, 1e-3) * 0.8)))
+        dt, fl = run(n)
+    desc = (f"oracle fwd+bwd (float64 NumPy) on the last {n} query rows of the longest "
+            f"sequence ({s1 - s0} tokens), all {w.hq} query heads, full key range")
+    return fl / dt / 1e12, dt, desc
+
+
+def cores_used() -> int:
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------ our arm
+
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "context_blockwise_attention_step_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import context_blockwise_attention_step_gb300 as ra
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ra.build()
+    w = W.NAMED[args.workload]
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    np_inputs = (q, k, v, do)
+    host = [torch.from_numpy(x).to(tdt).pin_memory() for x in np_inputs]
+    nat = [h.to(dev, non_blocking=True) for h in host]
+    prob = ra.problem_for(nat[0], nat[1], D=w.D, layout=w.layout, causal=w.causal,
+                          cu_seqlens=w.cu_seqlens if w.varlen else None)
+    qs, ks, vs, dos = (ra.shard_tokens(x, prob) for x in nat)
+    out = torch.empty_like(qs)
+    lse = torch.empty(ra.ops._lse_shape(prob), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)
+    ws = torch.empty(max(ra.workspace_bytes(prob), 1), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(x.numel() * x.element_size() for x in (qs, ks, vs, dos))
+    flush = None if in_bytes > 2 * L2_BYTES else torch.empty(2 * L2_BYTES // 4, device=dev)
+
+    for _ in range(args.warmup):
+        ra.ring_attn_fwd(qs, ks, vs, prob, out=out, lse=lse)
+        ra.ring_attn_bwd(dos, qs, ks, vs, out, lse, prob, dq=dq, dk=dk, dv=dv, workspace=ws)
+    torch.cuda.synchronize(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    st = [ev() for _ in range(args.steps)]
+    sp = [ev() for _ in range(args.steps)]
+    kf = [(ev(), ev()) for _ in range(args.steps)]
+    kb = [(ev(), ev()) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            st[i].record(stream)
+            ra.profile_events(*kf[i])
+            ra.ring_attn_fwd(qs, ks, vs, prob, out=out, lse=lse)
+            ra.profile_events(*kb[i])
+            ra.ring_attn_bwd(dos, qs, ks, vs, out, lse, prob, dq=dq, dk=dk, dv=dv, workspace=ws)
+            ra.profile_events(None, None)
+            sp[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(st, sp)]
+    fwd_ms = [a.elapsed_time(b) for a, b in kf]
+    bwd_ms = [a.elapsed_time(b) for a, b in kb]
+    if ra.check_device_status() != 0:
+        raise RuntimeError(f"device status after the timed region: {ra.last_error()}")
+
+    # ---- end to end: host buffers in, host buffers out, through the public API
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse, dq, dk, dv)]
+    dev_nat = [torch.empty_like(x) for x in nat]
+    dev_out_nat = [torch.empty_like(t) for t in (out, lse, dq, dk, dv)]
+
+    def e2e_step():
+        for h, d in zip(host, dev_nat):
+            d.copy_(h, non_blocking=True)
+        sm = [ra.shard_tokens(x, prob) for x in dev_nat]
+        o, l = ra.ring_attn_fwd(sm[0], sm[1], sm[2], prob)
+        g = ra.ring_attn_bwd(sm[3], sm[0], sm[1], sm[2], o, l, prob, workspace=ws)
+        ra.unshard_tokens(o, prob, out=dev_out_nat[0])
+        ra.unshard_lse(l, prob, out=dev_out_nat[1])
+        for t, d in zip(g, dev_out_nat[2:]):
+            ra.unshard_tokens(t, prob, out=d)
+        for d, h in zip(dev_out_nat, outs_h):
+            h.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = sum(h.numel() * h.element_size() for h in outs_h)
+
+    per = torch.tensor([sum(step_ms) / args.steps, e2e_ms, statistics.mean(fwd_ms),
+                        statistics.mean(bwd_ms)], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(per, op=dist.ReduceOp.MAX)
+    ms_step, e2e_ms, fwd_mean, bwd_mean = per.tolist()
+
+    ff, fb = fwd_bwd_flops(w)
+    value = world * (ff + fb) / (ms_step * 1e-3) / 1e12
+    e2e_value = world * (ff + fb) / (e2e_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    kern = {
+        "ring_fwd_tc": {"ms": fwd_mean, "tflops": ff / (fwd_mean * 1e-3) / 1e12,
+                        "algorithmic_tflop_per_launch": ff / 1e12},
+        "ring_bwd_tc": {"ms": bwd_mean, "tflops": fb / (bwd_mean * 1e-3) / 1e12,
+                        "algorithmic_tflop_per_launch": fb / 1e12},
+    }
+    for kv in kern.values():
+        kv["frac_of_sustained_peak"] = kv["tflops"] / peak_sus
+        kv["share_of_step"] = kv["ms"] / ms_step
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    src = {"ring_fwd_tc": "ra_fwd_tc.cu", "ring_bwd_tc": "ra_bwd_tc.cu"}[dom]
+    tr = TRAFFIC.get((dom, w.name))
+    traffic = tr["bytes"] if tr and tr["source_sha"] == kernel_source_hash(src) else None
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1:
+            v_cpu, t_cpu, desc = oracle_sample(w, args.cpu_seconds, np_inputs)
+            cpu = {"value": v_cpu, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                   "sample": desc, "seconds": t_cpu}
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded N(0,1), rounded to bf16)",
+            "config": {"workload": w.name, "batch": w.batch or None, "seq_len": w.seqlen or None,
+                       "total_tokens": w.total_tokens, "hq": w.hq, "hkv": w.hkv,
+                       "head_dim": w.head_dim, "D": w.D, "layout": w.layout, "causal": w.causal,
+                       "varlen": w.varlen, "parallelism": f"replicas{world}",
+                       "l2": ("inputs larger than L2" if flush is None
+                              else "L2 flushed between steps (outside the timed windows)"),
+                       "fwd_tflop": ff / 1e12, "bwd_tflop": fb / 1e12},
+            "pct_of_peak": 100.0 * value / world / peak_sus,
+            "tokens_per_s": world * w.total_tokens / (ms_step * 1e-3),
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": kern[dom]["tflops"],
+                         "peak": peak_sus, "peak_source": f"{peak_src} bf16_tflops_sustained",
+                         "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peak_sus,
+                         "traffic": traffic},
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks.summary(),
+            "step_ms": step_ms,
+        }
+    if dist is not None:
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.NAMED[args.workload]
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    inputs = (q, k, v, do)
+    per_step = max(5.0, min(args.cpu_seconds, 180.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step, inputs)
+    vals, secs, desc = [], [], ""
+    for _ in range(args.steps):
+        v_, t_, desc = oracle_sample(w, per_step, inputs)
+        vals.append(v_)
+        secs.append(t_)
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), rounded to bf16)",
+        "config": {"workload": w.name, "seq_len": w.seqlen or None, "total_tokens": w.total_tokens,
+                   "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim, "D": w.D,
+                   "layout": w.layout, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -10,5 +10,5 @@ from .ops import (  # noqa: F401
     Problem, make_problem, problem_for, ring_attn_fwd, ring_attn_bwd, block_attn_fwd,
     update_out_and_lse, workspace_bytes, shard_tokens, unshard_tokens, shard_lse, unshard_lse,
     validate, layout_positions, step_counts, work_items, check_device_status,
-    test_wait_timeout, last_error, version,
+    test_wait_timeout, profile_events, last_error, version,
 )

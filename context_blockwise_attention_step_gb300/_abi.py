@@ -26,7 +26,7 @@ EXPORTS = (
     "ra_ring_attn_fwd", "ra_block_attn_fwd", "ra_update_out_and_lse", "ra_workspace_bytes",
     "ra_ring_attn_bwd", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
     "ra_layout_positions", "ra_step_counts", "ra_work_items", "ra_check_device_status",
-    "ra_test_wait_timeout", "ra_last_error", "ra_version",
+    "ra_test_wait_timeout", "ra_profile_events", "ra_last_error", "ra_version",
 )
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
         "ra_work_items": (i32, [P, i32, vp, i32]),
         "ra_check_device_status": (i32, [i32]),
         "ra_test_wait_timeout": (i32, [ctypes.c_uint64, vp]),
+        "ra_profile_events": (i32, [vp, vp]),
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_version": (i32, []),
     }

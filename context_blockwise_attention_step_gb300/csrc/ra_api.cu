@@ -25,6 +25,16 @@ using ra::SeqDesc;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+// Records the profiling events (if set) around the launch done by `launch`.
+template <typename F>
+cudaError_t profiled(cudaStream_t st, F&& launch) {
+  if (g_prof_start) cudaEventRecord(g_prof_start, st);
+  const cudaError_t e = launch();
+  if (g_prof_stop) cudaEventRecord(g_prof_stop, st);
+  return e;
+}
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -205,8 +215,10 @@ int ra_ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const vo
   if (!q || !k || !v || !out || !lse) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
   PlanHolder P(make_plan(p, 0, 0, p->D, -1, p->dtype == RA_F32));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = use_tc(p) ? ra::launch_fwd_tc(*P.p, q, k, v, out, lse, st)
-                                  : ra::launch_fwd_simt(*P.p, p->dtype, q, k, v, out, lse, st);
+  const cudaError_t e = profiled(st, [&] {
+    return use_tc(p) ? ra::launch_fwd_tc(*P.p, q, k, v, out, lse, st)
+                     : ra::launch_fwd_simt(*P.p, p->dtype, q, k, v, out, lse, st);
+  });
   return e == cudaSuccess ? ok() : cuda_fail(e, "ring forward launch");
 }
 
@@ -269,12 +281,12 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
     e = cudaMemsetAsync(dq_acc, 0, dq_acc_bytes(p), st);
     if (e != cudaSuccess) return cuda_fail(e, "dq workspace clear");
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
-    e = ra::launch_bwd_tc(*P.p, q, k, v, dout, lse, delta, dq_acc, dk, dv, st);
+    e = profiled(st, [&] { return ra::launch_bwd_tc(*P.p, q, k, v, dout, lse, delta, dq_acc, dk, dv, st); });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     e = ra::launch_dq_convert(*E.p, dq_acc, dq, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward postprocess launch");
   } else {
-    e = ra::launch_bwd_simt(*E.p, p->dtype, q, k, v, dout, lse, delta, dq, dk, dv, st);
+    e = profiled(st, [&] { return ra::launch_bwd_simt(*E.p, p->dtype, q, k, v, dout, lse, delta, dq, dk, dv, st); });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
   return ok();
@@ -365,6 +377,14 @@ int ra_check_device_status(int reset) {
   if (e == cudaSuccess) e = ra::bwd_status(&b, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (f | b) return fail(RA_ERR_DEVICE_TIMEOUT, "device status: forward 0x%x backward 0x%x", f, b);
+  return ok();
+}
+
+int ra_profile_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(RA_ERR_INVALID_ARG, "pass both events or neither");
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
   return ok();
 }
 

@@ -240,6 +240,18 @@ def test_wait_timeout(timeout_ns: int, stream=None) -> int:
     return check(lib().ra_test_wait_timeout(timeout_ns, _stream(stream)))
 
 
+def profile_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event ``start`` / ``stop`` around the main kernel of the next
+    ring_attn_fwd / ring_attn_bwd calls (None, None switches the hook off)."""
+    if start is None:
+        check(lib().ra_profile_events(None, None))
+        return
+    for e in (start, stop):
+        if e.cuda_event == 0:  # torch creates events lazily
+            e.record()
+    check(lib().ra_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event)))
+
+
 def last_error() -> str:
     return lib().ra_last_error().decode()
 

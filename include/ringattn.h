@@ -182,6 +182,13 @@ int ra_check_device_status(int reset);
  * up, records RA_ERR_DEVICE_TIMEOUT in the device status and returns. */
 int ra_test_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/* Profiling hook: while set (non-NULL), ra_ring_attn_fwd and ra_ring_attn_bwd record
+ * `start_event` immediately before and `stop_event` immediately after their main kernel
+ * (the fused forward, or the backward's K/V-tile kernel) on the call's stream, so a caller
+ * can time that kernel alone with cudaEventElapsedTime. Both are cudaEvent_t handles owned
+ * by the caller; pass NULL, NULL to switch the hook off. Per calling thread. */
+int ra_profile_events(void* start_event, void* stop_event);
+
 /* Thread-local message describing the last error of this thread ("" if none). */
 const char* ra_last_error(void);
 
