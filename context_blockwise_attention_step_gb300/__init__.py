@@ -7,7 +7,8 @@ include/ringattn.h. This package is the thin Python binding over that ABI.
 from ._build import build  # noqa: F401
 from ._abi import RingAttnError, EXPORTS  # noqa: F401
 from .ops import (  # noqa: F401
-    Problem, make_problem, problem_for, ring_attn_fwd, ring_attn_bwd, block_attn_fwd,
+    Problem, make_problem, problem_for, ring_attn_fwd, ring_attn_bwd, ring_attn_bwd_noalloc,
+    block_attn_fwd,
     update_out_and_lse, workspace_bytes, shard_tokens, unshard_tokens, shard_lse, unshard_lse,
     validate, layout_positions, step_counts, work_items, check_device_status,
     test_wait_timeout, profile_events, last_error, version,

@@ -20,11 +20,12 @@ RA_F32 = 0
 RA_BF16 = 1
 LAYOUTS = {"basic": 0, "zigzag": 1, "stripe": 2}
 RA_MAX_SEQS = 1024
+RA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 # every symbol include/ringattn.h declares
 EXPORTS = (
     "ra_ring_attn_fwd", "ra_block_attn_fwd", "ra_update_out_and_lse", "ra_workspace_bytes",
-    "ra_ring_attn_bwd", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
+    "ra_ring_attn_bwd", "ra_ring_attn_bwd_noalloc", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
     "ra_layout_positions", "ra_step_counts", "ra_work_items", "ra_check_device_status",
     "ra_test_wait_timeout", "ra_profile_events", "ra_last_error", "ra_version",
 )
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
         "ra_update_out_and_lse": (i32, [P, i32, vp, vp, vp, i32, vp, vp]),
         "ra_workspace_bytes": (ctypes.c_size_t, [P, i32]),
         "ra_ring_attn_bwd": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]),
+        "ra_ring_attn_bwd_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "ra_shard_tokens": (i32, [P, i32, vp, vp, i64, vp]),
         "ra_shard_lse": (i32, [P, i32, vp, vp, vp]),
         "ra_validate": (i32, [P]),

@@ -198,6 +198,16 @@ size_t dq_acc_bytes(const ra_problem* p) {
 
 }  // namespace
 
+int ra::record_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
 extern "C" {
 
 int ra_version(void) { return RA_VERSION; }

@@ -87,18 +87,20 @@ __device__ __forceinline__ BwdWalk bwd_walk(const Plan& P, const BwdItem& it) {
   w.nqt = ceil_div(w.L, kQTileRows);
   w.pk0 = layout_pos(P.layout, P.D, w.L, it.j, w.b0);
   w.N = 0;
-  for (int s = 0; s < P.D; ++s) w.N += w.nqt - qt_begin(P, w, rank_at_step(P.D, it.j, s));
+  for (int r = 0; r < P.D; ++r) w.N += w.nqt - qt_begin(P, w, r);
   w.N *= P.group;
   return w;
 }
 
 // Calls f(r, h, q0) for every query tile the item visits, in walk order; stops early when
-// f returns false. Returns false if stopped.
+// f returns false. Returns false if stopped. The query ranks are walked in the same fixed
+// order 0..D-1 by every item (not in ring-step order relative to the item's shard): the
+// set of (rank, step) pairs and hence the sums are the same, but CTAs that run together
+// then read the same Q / dO tiles and add into the same dq rows at about the same time.
 template <typename F>
 __device__ __forceinline__ bool for_each_qtile(const Plan& P, const BwdItem& it, const BwdWalk& w,
                                                F&& f) {
-  for (int s = 0; s < P.D; ++s) {
-    const int r = rank_at_step(P.D, it.j, s);
+  for (int r = 0; r < P.D; ++r) {
     const int q_begin = qt_begin(P, w, r);
     for (int g = 0; g < P.group; ++g) {
       const int h = it.hk * P.group + g;

@@ -44,4 +44,7 @@ cudaError_t launch_shard_tokens(const Plan& P, int direction, const void* src, v
 cudaError_t launch_shard_lse(const Plan& P, int direction, const float* src, float* dst,
                              cudaStream_t st);
 
+// Sets the thread's ra_last_error() message (printf format) and returns `code`.
+int record_error(int code, const char* fmt, ...);
+
 }  // namespace ra

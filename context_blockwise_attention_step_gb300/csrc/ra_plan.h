@@ -84,15 +84,18 @@ RA_HD FwdItem decode_fwd(const Plan& P, int w) {
   return it;
 }
 
-// Backward decode: K/V tiles in increasing order (early keys are seen by the most
-// queries), shards next, K/V heads innermost.
+// Backward decode: K/V heads outermost, so that the CTAs running at the same time share
+// one K/V head and therefore add into the same query heads' dq rows (which then stay in
+// L2); within a head, K/V tiles in increasing order (early keys are seen by the most
+// queries), shards innermost.
 RA_HD BwdItem decode_bwd(const Plan& P, int w) {
   BwdItem it;
   it.seq = find_seq(P, w);
   const SeqDesc& s = P.seq[it.seq];
+  const int per_head = ceil_div(s.L, kKvTileRows) * P.D;
   int x = w - s.item_start;
-  it.hk = x % P.hkv;
-  x /= P.hkv;
+  it.hk = x / per_head;
+  x %= per_head;
   it.j = x % P.D;
   it.kt = x / P.D;
   return it;

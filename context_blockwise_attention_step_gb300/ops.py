@@ -173,6 +173,22 @@ def ring_attn_bwd(dout, q, k, v, out, lse, prob: Problem, dq=None, dk=None, dv=N
     return dq, dk, dv
 
 
+def ring_attn_bwd_noalloc(dout, q, k, v, out, lse, prob: Problem, dq, dk, dv, stream=None):
+    """ring_attn_bwd without a caller workspace, for callers that cannot allocate device
+    memory: the library's static scratch array is used (problems up to
+    RA_NOALLOC_SCRATCH_BYTES of scratch; calls overlapping on the GPU race on it). The
+    outputs dq, dk, dv must be passed in."""
+    r = prob.raw
+    nq, nk = prob.rows * r.hq * r.head_dim, prob.rows * r.hkv * r.head_dim
+    for t, n, name in ((dout, nq, "dout"), (q, nq, "q"), (k, nk, "k"), (v, nk, "v"),
+                       (out, nq, "out"), (dq, nq, "dq"), (dk, nk, "dk"), (dv, nk, "dv")):
+        _check_tensor(t, prob.token_dtype, n, name)
+    _check_tensor(lse, torch.float32, prob.rows * r.hq, "lse")
+    check(lib().ra_ring_attn_bwd_noalloc(prob.ptr, _p(q), _p(k), _p(v), _p(out), _p(lse),
+                                         _p(dout), _p(dq), _p(dk), _p(dv), _stream(stream)))
+    return dq, dk, dv
+
+
 def shard_tokens(x: torch.Tensor, prob: Problem, out=None, stream=None):
     """Natural order -> shard-major (bit-exact copy)."""
     out = torch.empty_like(x) if out is None else out

@@ -137,6 +137,23 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* The same backward for callers that cannot allocate device memory (a plain-C plugin
+ * handed only its input and output buffers, or a caller that must keep cudaMalloc and its
+ * device-wide synchronisation out of a training step). The pages have no counterpart: on
+ * the pages every rank allocates its own buffers. Instead of a caller workspace, the
+ * scratch (f32 dq partial sums and per-row dot(dout, out)) lives in one static device
+ * array of RA_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until exit.
+ * Arguments as for ra_ring_attn_bwd minus the workspace. Problems whose
+ * ra_workspace_bytes(p, 1) exceeds the array are rejected with RA_ERR_WORKSPACE and nothing
+ * is launched. The first call on a device looks the array's address up on that device
+ * (make that first call before any stream capture). Every call shares the array and the
+ * backward clears what must start at zero, but calls that overlap on the GPU race on it:
+ * order them on one stream. Allocates nothing. */
+#define RA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int ra_ring_attn_bwd_noalloc(const ra_problem* p, const void* q, const void* k, const void* v,
+                             const void* out, const float* lse, const void* dout, void* dq,
+                             void* dk, void* dv, void* stream);
+
 /* Natural order <-> shard-major order of a token tensor (row = one token, `row_bytes`
  * bytes: H*Dh*element size), bit-exact copy. direction 0: natural -> shard-major (shard);
  * 1: shard-major -> natural (unshard). src and dst must not overlap. */
