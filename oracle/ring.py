@@ -126,10 +126,14 @@ def ring_fwd(q, k, v, lengths, D: int, layout: str, causal: bool, varlen: bool,
 
 
 def ring_bwd(q, k, v, out, lse, dout, lengths, D: int, layout: str, causal: bool,
-             varlen: bool, scale: float | None = None):
+             varlen: bool, scale: float | None = None, steps=None, ranks=None):
     """Ring backward over shard-major tensors, using the final ``out`` and ``lse``.
 
-    Returns shard-major dq [T, Hq, Dh], dk and dv [T, Hkv, Dh].
+    Returns shard-major dq [T, Hq, Dh], dk and dv [T, Hkv, Dh]. ``steps`` and ``ranks``
+    (default: all) keep only the terms of those ring steps and query ranks, i.e. the block
+    gradients the unfused path adds one step at a time (how-to page, "Backward Pass and
+    Gradient Accumulation": dq += block_dq per step; block_dk / block_dv travel back to the
+    shard that owns the K/V).
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -147,9 +151,13 @@ def ring_bwd(q, k, v, out, lse, dout, lengths, D: int, layout: str, causal: bool
     for i, n in enumerate(lengths):
         pos = shard_positions(layout, D, n)
         for r in range(D):
+            if ranks is not None and r not in ranks:
+                continue
             rq = piece_rows(lengths, D, varlen, i, r)
             delta = (dout[rq] * out[rq]).sum(axis=2)  # [L, Hq]: rowsum(dO * O), final O
             for s in range(D):
+                if steps is not None and s not in steps:
+                    continue
                 j = (r - s) % D
                 rk = piece_rows(lengths, D, varlen, i, j)
                 allowed = ((pos[j][None, :] <= pos[r][:, None]) if causal

@@ -347,6 +347,43 @@ def test_ring_equals_single_pass(layout, D, causal, varlen):
         np.testing.assert_allclose(LY.unshard(got, rows, 0), ref, atol=1e-11)
 
 
+@pytest.mark.parametrize("layout", W.LAYOUTS)
+def test_per_step_backward_blocks(layout):
+    """The per-(rank, step) backward terms of the unfused path: the dk / dv a rank's step
+    adds into K/V shard (r - s) mod D are the gradient that rank's query rows alone give
+    those keys (plain definition restricted to the rank's rows), and summing the steps'
+    dq, dk, dv gives the whole gradient."""
+    rng = _rng(23)
+    D, lengths = 4, [48, 16]
+    q, k, v, do = _case(rng, lengths, 4, 2, 6, True)
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    rows = LY.shard_major_rows(layout, D, lengths, True)
+    sm = lambda x: LY.shard(x, rows, 0)
+    un = lambda x: LY.unshard(x, rows, 0)
+    out, lse = A.attention_fwd(q, k, v, cu, True)
+    dq, dk, dv = A.attention_bwd(q, k, v, do, cu, True)
+    o_s, l_s = sm(out), LY.shard(lse, rows, 1)
+    tot = [np.zeros_like(dq), np.zeros_like(dk), np.zeros_like(dv)]
+    for r in range(D):
+        # natural rows of rank r's query pieces
+        nat_rows = np.sort(np.concatenate([rows[R.piece_rows(lengths, D, True, i, r)]
+                                           for i in range(len(lengths))]))
+        _, dk_r, dv_r = A.attention_bwd(q, k, v, do, cu, True, rows=nat_rows)
+        for s in range(D):
+            g = R.ring_bwd(sm(q), sm(k), sm(v), o_s, l_s, sm(do), lengths, D, layout, True, True,
+                           steps=[s], ranks=[r])
+            j = (r - s) % D
+            kj = np.concatenate([R.piece_rows(lengths, D, True, i, j) for i in range(len(lengths))])
+            np.testing.assert_allclose(g[1][kj], sm(dk_r)[kj], atol=1e-12)
+            np.testing.assert_allclose(g[2][kj], sm(dv_r)[kj], atol=1e-12)
+            others = np.setdiff1d(np.arange(sum(lengths)), kj)
+            assert not g[1][others].any() and not g[2][others].any()
+            for acc, x in zip(tot, g):
+                acc += un(x)
+    for got, ref in zip(tot, (dq, dk, dv)):
+        np.testing.assert_allclose(got, ref, atol=1e-11)
+
+
 def test_partial_ring_resumes():
     """(out, lse) after k steps is the ring's whole state: merging the remaining steps'
     blocks into it gives the full result."""
