@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of one oracle sample")
+    ap.add_argument("--secondary", type=int, default=1,
+                    help="also time the unfused per-step path and the deterministic backward")
     return ap.parse_args()
 
 
@@ -73,11 +75,24 @@ def fwd_bwd_flops(w: W.Workload) -> tuple[float, float]:
 
 # ------------------------------------------------------------------------ CPU oracle sample
 
-def oracle_sample(w: W.Workload, target_s: float, inputs=None):
-    """Time the float64 oracle (forward + backward) on the last R query rows of the longest
-    sequence, every head; R grows until one sample takes about ``target_s`` / 4 or more.
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.uname().machine
 
-    Returns (TFLOP/s, seconds, description)."""
+
+def oracle_sample(w: W.Workload, target_s: float, inputs=None):
+    """Time the float64 oracle (forward + backward) on a stratified sample of query rows of
+    the longest sequence: R strata of equal length, one seeded random row in each, every
+    query head, each row against its whole causal key range. R doubles until one sample
+    takes about ``target_s`` / 4 or more.
+
+    Returns (TFLOP/s, seconds, description, extrapolated seconds of the full workload)."""
     from oracle import attention as A
 
     if inputs is None:
@@ -90,26 +105,32 @@ def oracle_sample(w: W.Workload, target_s: float, inputs=None):
     i = int(np.argmax(w.lengths))
     cu = w.cu_seqlens
     s0, s1 = int(cu[i]), int(cu[i + 1])
+    n_tok = s1 - s0
     qs, ks, vs, dos = q[s0:s1], k[s0:s1], v[s0:s1], do[s0:s1]
-    cu1 = np.array([0, s1 - s0])
+    cu1 = np.array([0, n_tok])
+    rng = np.random.default_rng(2024)
 
     def run(nrows):
-        rows = np.arange(s1 - s0 - nrows, s1 - s0)
+        edges = np.linspace(0, n_tok, nrows + 1).astype(np.int64)
+        rows = np.unique(np.array([rng.integers(a, max(a + 1, b)) for a, b in zip(edges[:-1], edges[1:])]))
         t0 = time.perf_counter()
         A.attention_fwd(qs, ks, vs, cu1, w.causal, rows=rows)
         A.attention_bwd(qs, ks, vs, dos, cu1, w.causal, rows=rows)
         dt = time.perf_counter() - t0
-        pairs = float(sum((r + 1) if w.causal else (s1 - s0) for r in rows)) * w.hq
-        return dt, 3.5 * 4.0 * w.head_dim * pairs
+        pairs = float(sum((r + 1) if w.causal else n_tok for r in rows)) * w.hq
+        return dt, 3.5 * 4.0 * w.head_dim * pairs, rows.size
 
-    n = 4
-    dt, fl = run(n)
-    while dt < target_s / 4 and n < (s1 - s0):
-        n = min(s1 - s0, max(n * 2, int(n * target_s / max(dt, 1e-3) * 0.8)))
-        dt, fl = run(n)
-    desc = (f"oracle fwd+bwd (float64 NumPy) on the last {n} query rows of the longest "
-            f"sequence ({s1 - s0} tokens), all {w.hq} query heads, full key range")
-    return fl / dt / 1e12, dt, desc
+    n = 8
+    dt, fl, got = run(n)
+    while dt < target_s / 4 and n < n_tok:
+        n = min(n_tok, max(n * 2, int(n * target_s / max(dt, 1e-3) * 0.8)))
+        dt, fl, got = run(n)
+    rate = fl / dt
+    full_s = sum(fwd_bwd_flops(w)) / rate
+    desc = (f"oracle fwd+bwd (float64 NumPy) on {got} query rows of the longest sequence "
+            f"({n_tok} tokens), one seeded row per equal stratum, all {w.hq} query heads, "
+            f"each row against its whole causal key range; CPU {cpu_model()}")
+    return rate / 1e12, dt, desc, full_s
 
 
 def cores_used() -> int:
@@ -270,6 +291,9 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(h.numel() * h.element_size() for h in host)
     d2h = sum(h.numel() * h.element_size() for h in outs_h)
 
+    merge = measure_merge(ra, prob, qs, lse, w, stream)
+    secondary = measure_secondary(ra, w, nat, prob, (qs, ks, vs, dos), ev, stream) if args.secondary else None
+
     per = torch.tensor([sum(step_ms) / args.steps, e2e_ms, statistics.mean(fwd_ms),
                         statistics.mean(bwd_ms)], device=dev, dtype=torch.float64)
     if dist is not None:
@@ -281,6 +305,12 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = world * (ff + fb) / (e2e_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak_burst = peaks["bf16_tflops"]
+    merge["frac_of_hbm"] = merge["gbs"] / peaks["hbm_gbs"]
+    merge["hbm_peak_gbs"] = peaks["hbm_gbs"]
+    mtr = TRAFFIC.get(("merge_kernel", w.name))
+    merge["traffic"] = (mtr["bytes"] if mtr and mtr["source_sha"] == kernel_source_hash("ra_misc.cu")
+                        else None)
     kern = {
         "ring_fwd_tc": {"ms": fwd_mean, "tflops": ff / (fwd_mean * 1e-3) / 1e12,
                         "algorithmic_tflop_per_launch": ff / 1e12},
@@ -289,6 +319,7 @@ def run_ours(args, rank, world, local_rank):
     }
     for kv in kern.values():
         kv["frac_of_sustained_peak"] = kv["tflops"] / peak_sus
+        kv["frac_of_burst_peak"] = kv["tflops"] / peak_burst
         kv["share_of_step"] = kv["ms"] / ms_step
     dom = max(kern, key=lambda n: kern[n]["ms"])
     src = {"ring_fwd_tc": "ra_fwd_tc.cu", "ring_bwd_tc": "ra_bwd_tc.cu"}[dom]
@@ -298,9 +329,10 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         cpu = None
         if world == 1:
-            v_cpu, t_cpu, desc = oracle_sample(w, args.cpu_seconds, np_inputs)
+            v_cpu, t_cpu, desc, full_s = oracle_sample(w, args.cpu_seconds, np_inputs)
             cpu = {"value": v_cpu, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
-                   "sample": desc, "seconds": t_cpu}
+                   "sample": desc, "seconds": t_cpu,
+                   "extrapolated_full_workload_s": full_s}
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -314,12 +346,18 @@ def run_ours(args, rank, world, local_rank):
                               else "L2 flushed between steps (outside the timed windows)"),
                        "fwd_tflop": ff / 1e12, "bwd_tflop": fb / 1e12},
             "pct_of_peak": 100.0 * value / world / peak_sus,
+            "pct_of_peak_burst": 100.0 * value / world / peak_burst,
+            "peak_tflops": {"sustained": peak_sus, "burst": peak_burst, "source": peak_src},
             "tokens_per_s": world * w.total_tokens / (ms_step * 1e-3),
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": kern[dom]["tflops"],
                          "peak": peak_sus, "peak_source": f"{peak_src} bf16_tflops_sustained",
                          "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peak_sus,
-                         "traffic": traffic},
+                         "frac_burst": kern[dom]["tflops"] / peak_burst,
+                         "traffic": traffic,
+                         "algorithmic_unit": "2.5 x 4 x head_dim FLOP per causal (query, key) pair"},
             "kernels": kern,
+            "merge_kernel": merge,
+            "secondary": secondary,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -330,6 +368,83 @@ def run_ours(args, rank, world, local_rank):
     if dist is not None:
         dist.destroy_process_group()
     return result
+
+
+def measure_merge(ra, prob, qs, lse, w, stream, reps=5):
+    """HBM GB/s of the standalone update_out_and_lse kernel on the workload's rows: float32
+    out / lse updated in place with a bf16 block. Algorithmic bytes per (token, head) row:
+    read + write out (2 x 4 x Dh), read the bf16 block (2 x Dh), read + write lse and read
+    the block lse (12): 1292 B at Dh = 128."""
+    import torch
+
+    out = torch.zeros(qs.shape, device=qs.device, dtype=torch.float32)
+    mlse = torch.full(lse.shape, float("-inf"), device=qs.device, dtype=torch.float32)
+    block = torch.randn(qs.shape, device=qs.device, dtype=torch.float32).to(torch.bfloat16)
+    blse = torch.randn(lse.shape, device=qs.device, dtype=torch.float32)
+    for _ in range(2):
+        ra.update_out_and_lse(out, mlse, block, blse, prob)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+    for i in range(reps):
+        ev[2 * i].record(stream)
+        ra.update_out_and_lse(out, mlse, block, blse, prob)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(reps))
+    rows = w.total_tokens * w.hq
+    per_row = 2 * 4 * w.head_dim + 2 * w.head_dim + 12
+    del out, mlse, block, blse
+    return {"ms": ms, "bytes_per_launch": rows * per_row, "bytes_per_row": per_row,
+            "gbs": rows * per_row / (ms * 1e-3) / 1e9, "launches_timed": reps}
+
+
+def measure_secondary(ra, w, nat, prob, sm, ev, stream, reps=2):
+    """TFLOP/s of (a) the unfused path: D block forwards merged one step at a time, then D
+    per-step block backwards added into float32 accumulators; (b) the deterministic
+    backward (K/V-tile pass without dq + query-tile dq pass). Same algorithmic FLOP as the
+    fused step."""
+    import torch
+
+    qs, ks, vs, dos = sm
+    ff, fb = fwd_bwd_flops(w)
+    out, lse = ra.ring_attn_fwd(qs, ks, vs, prob)
+    lse_shape = lse.shape
+    res = {}
+
+    def unfused():
+        o = torch.zeros(qs.shape, device=qs.device, dtype=torch.float32)
+        l = torch.full(lse_shape, float("-inf"), device=qs.device, dtype=torch.float32)
+        bo = torch.empty(qs.shape, device=qs.device, dtype=torch.bfloat16)
+        bl = torch.empty(lse_shape, device=qs.device, dtype=torch.float32)
+        for s in range(w.D):
+            ra.block_attn_fwd(qs, ks, vs, prob, rank=-1, step=s, out_dtype=torch.bfloat16,
+                              block_out=bo, block_lse=bl)
+            ra.update_out_and_lse(o, l, bo, bl, prob)
+        acc = [torch.zeros(t.shape, device=qs.device, dtype=torch.float32) for t in (qs, ks, vs)]
+        for s in range(w.D):
+            ra.block_attn_bwd(dos, qs, ks, vs, out, lse, prob, -1, s, *acc)
+
+    det = ra.problem_for(nat[0], nat[1], D=w.D, layout=w.layout, causal=w.causal,
+                         cu_seqlens=w.cu_seqlens if w.varlen else None, deterministic=True)
+    ws = torch.empty(max(ra.workspace_bytes(det), 1), device=qs.device, dtype=torch.uint8)
+
+    def deterministic():
+        ra.ring_attn_bwd(dos, qs, ks, vs, out, lse, det, workspace=ws)
+
+    for name, fn, flop in (("unfused_fwd_bwd", unfused, ff + fb), ("deterministic_bwd", deterministic, fb)):
+        fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        res[name] = {"ms": ms, "tflops": flop / (ms * 1e-3) / 1e12}
+    if ra.check_device_status() != 0:
+        raise RuntimeError(f"device status after the secondary measurements: {ra.last_error()}")
+    return res
 
 
 # ------------------------------------------------------------------------ reference arm
@@ -346,7 +461,7 @@ def run_reference(args, rank, world):
         oracle_sample(w, per_step, inputs)
     vals, secs, desc = [], [], ""
     for _ in range(args.steps):
-        v_, t_, desc = oracle_sample(w, per_step, inputs)
+        v_, t_, desc, _ = oracle_sample(w, per_step, inputs)
         vals.append(v_)
         secs.append(t_)
     value = statistics.mean(vals)

@@ -25,9 +25,10 @@ RA_NOALLOC_SCRATCH_BYTES = 64 << 20
 # every symbol include/ringattn.h declares
 EXPORTS = (
     "ra_ring_attn_fwd", "ra_block_attn_fwd", "ra_update_out_and_lse", "ra_workspace_bytes",
-    "ra_ring_attn_bwd", "ra_ring_attn_bwd_noalloc", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
+    "ra_ring_attn_bwd", "ra_block_attn_bwd", "ra_ring_attn_bwd_noalloc", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
     "ra_layout_positions", "ra_step_counts", "ra_work_items", "ra_check_device_status",
-    "ra_test_wait_timeout", "ra_profile_events", "ra_last_error", "ra_version",
+    "ra_test_wait_timeout", "ra_test_exp2_poly", "ra_profile_events", "ra_last_error",
+    "ra_version",
 )
 
 
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         "ra_workspace_bytes": (ctypes.c_size_t, [P, i32]),
         "ra_ring_attn_bwd": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]),
         "ra_ring_attn_bwd_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "ra_block_attn_bwd": (i32, [P, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    ctypes.c_size_t, vp]),
         "ra_shard_tokens": (i32, [P, i32, vp, vp, i64, vp]),
         "ra_shard_lse": (i32, [P, i32, vp, vp, vp]),
         "ra_validate": (i32, [P]),
@@ -85,6 +88,7 @@ def lib() -> ctypes.CDLL:
         "ra_work_items": (i32, [P, i32, vp, i32]),
         "ra_check_device_status": (i32, [i32]),
         "ra_test_wait_timeout": (i32, [ctypes.c_uint64, vp]),
+        "ra_test_exp2_poly": (i32, [vp, vp, i32, vp]),
         "ra_profile_events": (i32, [vp, vp]),
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_version": (i32, []),

@@ -114,7 +114,7 @@ int validate(const ra_problem* p) {
 
 // which: 0 forward items, 1 backward items, 2 no items (elementwise kernels).
 Plan* make_plan(const ra_problem* p, int which, int step_begin, int step_end, int rank_only,
-                int out_f32, std::vector<int>* natural_index = nullptr) {
+                int out_f32, std::vector<int>* natural_index = nullptr, int kv_shard_only = -1) {
   Plan* P = static_cast<Plan*>(calloc(1, sizeof(Plan)));
   P->layout = p->layout;
   P->causal = p->causal ? 1 : 0;
@@ -126,9 +126,12 @@ Plan* make_plan(const ra_problem* p, int which, int step_begin, int step_end, in
   P->step_begin = step_begin;
   P->step_end = step_end;
   P->rank_only = rank_only;
+  P->kv_shard_only = kv_shard_only;
   P->out_f32 = out_f32;
+  P->bwd_accum = 0;
   P->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
   P->scale_log2 = P->scale * 1.4426950408889634f;
+  P->dq_mul = P->scale;
   P->timeout_ns = ra::kDefaultTimeoutNs;
   const std::vector<int64_t> len = lengths_of(p);
   const int n = static_cast<int>(len.size());
@@ -266,8 +269,10 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
 }
 
 size_t ra_workspace_bytes(const ra_problem* p, int which) {
-  if (validate(p) != RA_OK || which != 1) return 0;
-  return delta_bytes(p) + dq_acc_bytes(p);
+  if (validate(p) != RA_OK) return 0;
+  if (which == 1) return delta_bytes(p) + dq_acc_bytes(p);
+  if (which == 2) return delta_bytes(p);
+  return 0;
 }
 
 int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const void* v,
@@ -286,12 +291,23 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
   PlanHolder E(make_plan(p, 2, 0, p->D, -1, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  if (use_tc(p) && !p->deterministic) {
+  if (use_tc(p) && p->deterministic) {
+    // dk, dv from the K/V-tile kernel without its dq part; dq query-tile-major
+    PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
+    e = profiled(st, [&] {
+      return ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvOnly, q, k, v, dout, lse, delta, nullptr, dk, dv, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    e = ra::launch_bwd_dq_tc(*P.p, q, k, v, dout, lse, delta, dq, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward dq launch");
+  } else if (use_tc(p)) {
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(p));
     e = cudaMemsetAsync(dq_acc, 0, dq_acc_bytes(p), st);
     if (e != cudaSuccess) return cuda_fail(e, "dq workspace clear");
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
-    e = profiled(st, [&] { return ra::launch_bwd_tc(*P.p, q, k, v, dout, lse, delta, dq_acc, dk, dv, st); });
+    e = profiled(st, [&] {
+      return ra::launch_bwd_tc(*P.p, ra::BwdKind::kFused, q, k, v, dout, lse, delta, dq_acc, dk, dv, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     e = ra::launch_dq_convert(*E.p, dq_acc, dq, st);
     if (e != cudaSuccess) return cuda_fail(e, "backward postprocess launch");
@@ -300,6 +316,40 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   }
   return ok();
+}
+
+int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, const void* k,
+                      const void* v, const void* out, const float* lse, const void* dout,
+                      float* dq_acc, float* dk_acc, float* dv_acc, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (int e = validate(p)) return e;
+  if (!q || !k || !v || !out || !lse || !dout || !dq_acc || !dk_acc || !dv_acc)
+    return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (rank >= p->D || rank < -1) return fail(RA_ERR_INVALID_ARG, "rank %d out of range", rank);
+  if (step < 0 || step >= p->D) return fail(RA_ERR_INVALID_ARG, "step %d out of range", step);
+  const size_t need = delta_bytes(p);
+  if (workspace_bytes < need)
+    return fail(RA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(RA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  const int r_only = rank < 0 ? -1 : rank;
+  const int kv_only = rank < 0 ? -1 : ((rank - step) % p->D + p->D) % p->D;
+  PlanHolder E(make_plan(p, 2, step, step + 1, r_only, 0));
+  cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  if (use_tc(p)) {
+    PlanHolder P(make_plan(p, 1, step, step + 1, r_only, 0, nullptr, kv_only));
+    P.p->bwd_accum = 1;
+    e = ra::launch_bwd_tc(*P.p, ra::BwdKind::kBlockAccum, q, k, v, dout, lse, delta, dq_acc, dk_acc,
+                          dv_acc, st);
+  } else {
+    PlanHolder P(make_plan(p, 2, step, step + 1, r_only, 0, nullptr, kv_only));
+    P.p->bwd_accum = 1;
+    e = ra::launch_bwd_simt(*P.p, p->dtype, q, k, v, dout, lse, delta, dq_acc, dk_acc, dv_acc, st);
+  }
+  return e == cudaSuccess ? ok() : cuda_fail(e, "block backward launch");
 }
 
 int ra_shard_tokens(const ra_problem* p, int direction, const void* src, void* dst,
@@ -382,11 +432,13 @@ int ra_work_items(const ra_problem* p, int which, int32_t* items_out, int max_it
 int ra_check_device_status(int reset) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
-  unsigned int f = 0, b = 0;
+  unsigned int f = 0, b = 0, d = 0;
   e = ra::fwd_status(&f, reset != 0);
   if (e == cudaSuccess) e = ra::bwd_status(&b, reset != 0);
+  if (e == cudaSuccess) e = ra::bwd_dq_status(&d, reset != 0);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
-  if (f | b) return fail(RA_ERR_DEVICE_TIMEOUT, "device status: forward 0x%x backward 0x%x", f, b);
+  if (f | b | d)
+    return fail(RA_ERR_DEVICE_TIMEOUT, "device status: forward 0x%x backward 0x%x dq 0x%x", f, b, d);
   return ok();
 }
 
@@ -403,6 +455,13 @@ int ra_test_wait_timeout(uint64_t timeout_ns, void* stream) {
     return fail(RA_ERR_INVALID_ARG, "timeout must be in (0, 10 s]");
   const cudaError_t e = ra::launch_wait_timeout(timeout_ns, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e, "wait-timeout launch");
+}
+
+int ra_test_exp2_poly(const float* x, float* y, int n, void* stream) {
+  if (!x || !y || n < 0) return fail(RA_ERR_INVALID_ARG, "bad arguments");
+  if (n == 0) return ok();
+  const cudaError_t e = ra::launch_exp2_poly(x, y, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "exp2 test launch");
 }
 
 }  // extern "C"

@@ -9,22 +9,32 @@
 // every query head of the GQA group, and every 128-row query tile of shard r that may see
 // the tile (global-position causal rule). With P^T computed K/V-row-major:
 //
-//   S^T  = K Q^T                 tcgen05 (SS), TMEM
-//   P^T  = 2^(S^T*scale*log2e - lse*log2e)  (recomputed from lse, masked), bf16 -> TMEM
-//   dP^T = V dO^T                tcgen05 (SS), TMEM
-//   dV  += P^T dO                tcgen05 (TS: P^T from TMEM), f32 in TMEM for the whole walk
-//   dS^T = P^T * (dP^T - delta)  delta = rowsum(dO * O) from the preprocess kernel; bf16 smem
-//   dK  += dS^T Q                tcgen05 (SS), f32 in TMEM for the whole walk
-//   dQ   = dS K                  tcgen05 (SS, dS read MN-major), then added with vector
-//                                float atomics into an f32 dq workspace
+//   S^T  = K Q^T                 tcgen05 (SS), TMEM buffer X
+//   P^T  = 2^(S^T*scale*log2e - lse*log2e)  (recomputed from lse, masked), bf16 -> X
+//                                (columns [32, 96), over S^T columns already consumed)
+//   dP^T = V dO^T                tcgen05 (SS), TMEM buffer Y
+//   dV  += P^T dO                tcgen05 (TS: P^T from X), f32 in TMEM for the whole walk
+//   dS^T = P^T * (dP^T - delta)  delta = rowsum(dO * O) from the preprocess kernel; bf16,
+//                                written to Y (over the consumed dP^T) and to smem
+//   dK  += dS^T Q                tcgen05 (TS: dS^T from Y), f32 in TMEM for the whole walk
+//   dQ   = dS K                  tcgen05 (SS, dS read MN-major from smem) into Y, then
+//                                added with vector float reductions into f32 dq sums
 //
-// dK and dV leave TMEM once per tile (times scale for dK), so they need no atomics; dq is
-// scaled and converted by the postprocess kernel.
+// The MMA warp issues, per query tile i: dV(i), dP(i), S(i+1), dK(i), dQ(i). P(i) stays
+// in the registers of the threads that computed it, so X is free for S(i+1) as soon as
+// dV(i) is issued, and the softmax threads compute P(i+1) while the tensor core runs dK(i)
+// and dQ(i); the drain of dQ(i) overlaps dV(i+1). The lse and delta of each query tile
+// are staged in shared memory ahead of use by a loader warp.
 //
-// Warp roles (384 threads): warp 0 TMA producer (K, V once per item; Q and dO per query
-// tile, two stages), warp 1 TMEM allocator + MMA issuer, warps 4-7 the P / dS warpgroup
-// (thread = K/V row) which also writes dK and dV, warps 8-11 the dQ warpgroup
-// (thread = query row).
+// Variants (template): kWithDQ = false leaves dq out (the K/V pass of the deterministic
+// backward); kAccum = true adds float32 dk / dv into the outputs instead of storing them
+// in the problem dtype (the per-step block backward of the unfused path).
+//
+// Warp roles (512 threads): warp 0 TMA producer (K, V once per item; Q and dO per query
+// tile, two stages), warp 1 TMEM allocator + MMA issuer, warp 2 lse / delta loader,
+// warps 4-7 and 8-11 the P / dS warpgroups (thread = K/V row; query columns 0-63 and
+// 64-127; at the end of an item they write dK and dV respectively), warps 12-15 the dQ
+// warpgroup (thread = query row).
 #include <cuda_runtime.h>
 
 #include "ra_internal.h"
@@ -37,7 +47,7 @@ static __device__ unsigned int g_status_bwd;
 
 namespace {
 
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 constexpr int kSubBytes = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -50,24 +60,25 @@ struct BwdCfg {
   static constexpr int kOffQ = kOffV + kTileBytes;            // 2 stages: Q then dO
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kOffDS = kOffQ + 2 * kStageBytes;     // 128 x 128 bf16
-  static constexpr int kOffLse = kOffDS + 2 * kSubBytes;     // [2][128] f32
-  static constexpr int kOffDelta = kOffLse + 2 * 128 * 4;    // [2][128] f32
-  static constexpr int kOffBar = kOffDelta + 2 * 128 * 4;
-  static constexpr int kSmemBytes = kOffBar + 320;
+  static constexpr int kOffLs = kOffDS + 2 * kSubBytes;      // [2 slots][-lse*log2e | delta][128]
+  static constexpr int kOffBar = kOffLs + 2 * 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + 192;
   static constexpr int kKSteps = DH / 16;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColDK = 0, kColDV = DH, kColS = 2 * DH, kColDP = 2 * DH + 128;
+  static constexpr uint32_t kColDK = 0, kColDV = DH, kColX = 2 * DH, kColY = 2 * DH + 128;
 };
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_free;
-  uint64_t acc_done, acc_free, drain;
-  uint64_t lse_bar[2];
+  uint64_t ls_full[2], ls_empty[2];
+  uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
+  uint64_t acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(BwdBars) <= 192, "barrier block");
+static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 
 struct BwdWalk {
   int L, b0, N, nqt;
@@ -87,7 +98,8 @@ __device__ __forceinline__ BwdWalk bwd_walk(const Plan& P, const BwdItem& it) {
   w.nqt = ceil_div(w.L, kQTileRows);
   w.pk0 = layout_pos(P.layout, P.D, w.L, it.j, w.b0);
   w.N = 0;
-  for (int r = 0; r < P.D; ++r) w.N += w.nqt - qt_begin(P, w, r);
+  for (int r = 0; r < P.D; ++r)
+    if (rank_in_walk(P, it.j, r)) w.N += w.nqt - qt_begin(P, w, r);
   w.N *= P.group;
   return w;
 }
@@ -101,6 +113,7 @@ template <typename F>
 __device__ __forceinline__ bool for_each_qtile(const Plan& P, const BwdItem& it, const BwdWalk& w,
                                                F&& f) {
   for (int r = 0; r < P.D; ++r) {
+    if (!rank_in_walk(P, it.j, r)) continue;
     const int q_begin = qt_begin(P, w, r);
     for (int g = 0; g < P.group; ++g) {
       const int h = it.hk * P.group + g;
@@ -125,15 +138,89 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
   }
 }
 
-template <int DH>
+__device__ __forceinline__ void add_row32_f32(float* dst, const uint32_t (&r)[32], float mul) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float4 o = d[q];
+    o.x += __uint_as_float(r[4 * q + 0]) * mul;
+    o.y += __uint_as_float(r[4 * q + 1]) * mul;
+    o.z += __uint_as_float(r[4 * q + 2]) * mul;
+    o.w += __uint_as_float(r[4 * q + 3]) * mul;
+    d[q] = o;
+  }
+}
+
+// One 32-column chunk of dS^T = P^T * (dP^T - delta) for the query columns
+// [c0 + 32*CH, c0 + 32*CH + 32) of this thread's K/V row: reads dP^T from Y, writes the
+// bf16 result to Y columns [32 + c0/2 + 16*CH, +16) (the A operand of the dK MMA) and,
+// when dQ is computed, to the 128B-swizzled smem tile (the A operand of the dQ MMA).
+template <int CH, bool kWithDQ>
+__device__ __forceinline__ void ds_chunk(uint32_t tY, int c0, const float* dl,
+                                         const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
+  const int cs = c0 + 32 * CH;
+  uint32_t dp[32], o[16];
+  tmem_ld32(tY + cs, dp);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 d2 = *reinterpret_cast<const float2*>(dl + cs + 2 * i);
+    uint64_t x = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), f2(d2.x, d2.y));
+    x = mul2(x, f2_of_bf16x2(pp[16 * CH + i]));
+    o[i] = bf16x2_of(x);
+  }
+  tmem_st16(tY + 32 + c0 / 2 + 16 * CH, o);
+  if constexpr (kWithDQ) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int chunk = 4 * CH + q;
+      uint4 v;
+      v.x = o[4 * q + 0];
+      v.y = o[4 * q + 1];
+      v.z = o[4 * q + 2];
+      v.w = o[4 * q + 3];
+      *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = v;
+    }
+  }
+}
+
+// One 32-column chunk of P^T = 2^(S^T * scale*log2e - lse*log2e) for query columns
+// [c0 + 32*CH, +32): columns before `lo` (queries that may not see this key) are zero;
+// columns past the sequence piece have -lse*log2e = -inf from the loader and give 0.
+// The bf16 result goes to X columns [32 + c0/2 + 16*CH, +16): inside the S^T columns this
+// warpgroup reads itself (the other warpgroup may still be reading its own), on columns
+// of a chunk this thread has already read (hence the per-warpgroup chunk order).
+template <int CH>
+__device__ __forceinline__ void p_chunk(uint32_t tX, int c0, const float* nl, uint64_t sl2x2,
+                                        int lo, uint32_t (&pp)[32]) {
+  const int cs = c0 + 32 * CH;
+  uint32_t sv[32], pk[16];
+  tmem_ld32(tX + cs, sv);
+  const bool full = __all_sync(0xffffffffu, lo <= cs);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 n2 = *reinterpret_cast<const float2*>(nl + cs + 2 * i);
+    const float2 e = f2_split(
+        fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, f2(n2.x, n2.y)));
+    float p0 = ex2(e.x), p1 = ex2(e.y);
+    if (!full) {
+      if (cs + 2 * i < lo) p0 = 0.f;
+      if (cs + 2 * i + 1 < lo) p1 = 0.f;
+    }
+    pk[i] = pack_bf16x2(p0, p1);
+    pp[16 * CH + i] = pk[i];
+  }
+  tmem_st16(tX + 32 + c0 / 2 + 16 * CH, pk);
+}
+
+template <int DH, bool kWithDQ, bool kAccum>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ring_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ Plan P,
                        const float* __restrict__ lse, const float* __restrict__ delta,
-                       float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
-                       __nv_bfloat16* __restrict__ dv) {
+                       float* __restrict__ dq_acc, void* __restrict__ dk_out,
+                       void* __restrict__ dv_out) {
   using C = BwdCfg<DH>;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars& sh = *reinterpret_cast<BwdBars*>(smem + C::kOffBar);
@@ -152,19 +239,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.q_full[i], 1);
       mbar_init(&sh.q_empty[i], 1);
+      mbar_init(&sh.ls_full[i], 32);
+      mbar_init(&sh.ls_empty[i], 256);
     }
     mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.p_full, 256);
     mbar_init(&sh.dp_full, 1);
-    mbar_init(&sh.p_full, 128);
-    mbar_init(&sh.ds_full, 128);
-    mbar_init(&sh.ds_empty, 1);
+    mbar_init(&sh.ds_full, 256);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 128);
     mbar_init(&sh.acc_done, 1);
-    mbar_init(&sh.acc_free, 128);
     mbar_init(&sh.drain, 1);
-    mbar_init(&sh.lse_bar[0], 128);
-    mbar_init(&sh.lse_bar[1], 128);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -221,13 +306,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t kv_phase = 0, af_phase = 0, p_phase = 0, ds_phase = 0, dqf_phase = 0;
-      int qcount = 0;
+      uint32_t kv_phase = 0, p_phase = 0, ds_phase = 0, dqf_phase = 0;
+      int qc = 0;
+      bool dq_pending = false;
       const uint32_t idSS = idesc_bf16_f32(128, 128, 0, 0);     // S^T, dP^T
-      const uint32_t idKV = idesc_bf16_f32(128, DH, 0, 1);      // dV, dK: B MN-major
+      const uint32_t idKV = idesc_bf16_f32(128, DH, 0, 1);      // dV, dK: A from TMEM, B MN-major
       const uint32_t idQ = idesc_bf16_f32(128, DH, 1, 1);       // dQ: A and B MN-major
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       const uint32_t sQ0 = smem_u32(smem + C::kOffQ), sDS = smem_u32(smem + C::kOffDS);
+      const uint32_t tX = tmem + C::kColX, tY = tmem + C::kColY;
+      auto issue_S = [&](uint32_t sQ) {
+#pragma unroll
+        for (int k = 0; k < C::kKSteps; ++k) {
+          const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+          mma_ss(tX, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idSS, k > 0);
+        }
+        tc_commit(&sh.s_full);
+      };
       bool ok = true;
       for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
         const BwdItem it = decode_bwd(P, w);
@@ -235,90 +330,121 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (wk.N == 0) continue;
         if (!(ok = mbar_wait(&sh.kv_full, kv_phase, abort_flag, tmo, status))) break;
         kv_phase ^= 1;
-        // the previous item's dK / dV must be out of TMEM before accumulate = 0 overwrites
-        if (!(ok = mbar_wait(&sh.acc_free, af_phase ^ 1, abort_flag, tmo, status))) break;
-        af_phase ^= 1;
-        tc_fence_after();
+        {
+          const int st = qc & 1;
+          if (!(ok = mbar_wait(&sh.q_full[st], (qc >> 1) & 1, abort_flag, tmo, status))) break;
+          tc_fence_after();
+          issue_S(sQ0 + st * C::kStageBytes);
+        }
         int i = 0;
         ok = for_each_qtile(P, it, wk, [&](int, int, int) -> bool {
-          const int st = qcount & 1;
-          const uint32_t ph = (qcount >> 1) & 1;
+          const int qi = qc + i;
+          const int st = qi & 1;
           const uint32_t sQ = sQ0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
-          if (!mbar_wait(&sh.q_full[st], ph, abort_flag, tmo, status)) return false;
-          tc_fence_after();
-          // S^T = K Q^T
-#pragma unroll
-          for (int k = 0; k < C::kKSteps; ++k) {
-            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
-                   idSS, k > 0);
-          }
-          tc_commit(&sh.s_full);
-          // dP^T = V dO^T (its TMEM columns held the previous dQ)
-          if (i > 0) {
-            if (!mbar_wait(&sh.dq_free, dqf_phase, abort_flag, tmo, status)) return false;
-            dqf_phase ^= 1;
-            tc_fence_after();
-          }
-#pragma unroll
-          for (int k = 0; k < C::kKSteps; ++k) {
-            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColDP, sdesc_sw128(sV + off, 16, 1024),
-                   sdesc_sw128(sDO + off, 16, 1024), idSS, k > 0);
-          }
-          tc_commit(&sh.dp_full);
-          // dV += P^T dO
+          // dV += P^T dO (P^T from X columns [32, 96)). dV is overwritten at the first tile:
+          // the previous item's dK / dV were read by the P / dS threads before they
+          // signalled P(0).
           if (!mbar_wait(&sh.p_full, p_phase, abort_flag, tmo, status)) return false;
           p_phase ^= 1;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + 8 * k,
-                   sdesc_sw128(sDO + k * 2048, kSubBytes, 1024), idKV, (i > 0 || k > 0) ? 1u : 0u);
-          // dK += dS^T Q ; dQ = dS K
+            mma_ts(tmem + C::kColDV, tX + 32 + 8 * k, sdesc_sw128(sDO + k * 2048, kSubBytes, 1024),
+                   idKV, (i > 0 || k > 0) ? 1u : 0u);
+          // dP^T = V dO^T into Y, once the previous dQ has been read out of Y
+          if (dq_pending) {
+            if (!mbar_wait(&sh.dq_free, dqf_phase, abort_flag, tmo, status)) return false;
+            dqf_phase ^= 1;
+            dq_pending = false;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int k = 0; k < C::kKSteps; ++k) {
+            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+            mma_ss(tY, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, k > 0);
+          }
+          tc_commit(&sh.dp_full);
+          // S(i+1) into X: P(i) has been read by dV(i) (issued above, executed in order)
+          if (i + 1 < wk.N) {
+            const int st1 = (qi + 1) & 1;
+            if (!mbar_wait(&sh.q_full[st1], ((qi + 1) >> 1) & 1, abort_flag, tmo, status)) return false;
+            tc_fence_after();
+            issue_S(sQ0 + st1 * C::kStageBytes);
+          }
+          // dK += dS^T Q (dS^T from Y) ; dQ = dS K into Y
           if (!mbar_wait(&sh.ds_full, ds_phase, abort_flag, tmo, status)) return false;
           ds_phase ^= 1;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
-                   sdesc_sw128(sQ + k * 2048, kSubBytes, 1024), idKV, (i > 0 || k > 0) ? 1u : 0u);
-          }
-#pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ss(tmem + C::kColDP, sdesc_sw128(sDS + k * 2048, kSubBytes, 1024),
-                   sdesc_sw128(sK + k * 2048, kSubBytes, 1024), idQ, k > 0);
-          tc_commit(&sh.dq_full);
-          tc_commit(&sh.ds_empty);
+            mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQ + k * 2048, kSubBytes, 1024), idKV,
+                   (i > 0 || k > 0) ? 1u : 0u);
+          if constexpr (kWithDQ) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tY, sdesc_sw128(sDS + k * 2048, kSubBytes, 1024),
+                     sdesc_sw128(sK + k * 2048, kSubBytes, 1024), idQ, k > 0);
+            tc_commit(&sh.dq_full);
+            dq_pending = true;
+          }
           tc_commit(&sh.q_empty[st]);
-          ++qcount;
           ++i;
           return true;
         });
         if (!ok) break;
+        qc += wk.N;
         tc_commit(&sh.acc_done);
         tc_commit(&sh.kv_empty);
-        // the last dQ must be read before the next item's first dP reuses its columns
-        if (!(ok = mbar_wait(&sh.dq_free, dqf_phase, abort_flag, tmo, status))) break;
-        dqf_phase ^= 1;
       }
       tc_commit(&sh.drain);
       mbar_wait(&sh.drain, 0, abort_flag, tmo, status);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------------ P / dS warpgroup
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ lse / delta loader
+    float* ls_base = reinterpret_cast<float*>(smem + C::kOffLs);
+    int t = 0;
+    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+      const BwdItem it = decode_bwd(P, w);
+      const BwdWalk wk = bwd_walk(P, it);
+      if (wk.N == 0) continue;
+      const SeqDesc& sd = P.seq[it.seq];
+      const bool ok = for_each_qtile(P, it, wk, [&](int r, int h, int q0) -> bool {
+        const int slot = t & 1;
+        if (!mbar_wait(&sh.ls_empty[slot], ((t >> 1) & 1) ^ 1, abort_flag, tmo, status)) return false;
+        float* nl = ls_base + slot * 256;
+        const size_t li0 = sd.lse_off + static_cast<size_t>(h) * P.lse_hstride +
+                           static_cast<size_t>(r) * P.shard_stride + q0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = lane + 32 * k;
+          float n = -INFINITY, d = 0.f;
+          if (q0 + c < wk.L) {
+            const float l = lse[li0 + c];
+            n = l == -INFINITY ? -INFINITY : -l * kLog2e;
+            d = delta[li0 + c];
+          }
+          nl[c] = n;
+          nl[128 + c] = d;
+        }
+        mbar_arrive(&sh.ls_full[slot]);
+        ++t;
+        return true;
+      });
+      if (!ok) break;
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------------ P / dS warpgroups
+    const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // K/V row within the tile = TMEM lane
+    const int c0 = wg * 64;               // this warpgroup's query columns
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kColS, tDP = tmem + lane_off + C::kColDP;
-    const uint32_t tDK = tmem + lane_off + C::kColDK, tDV = tmem + lane_off + C::kColDV;
-    float* lse_s = reinterpret_cast<float*>(smem + C::kOffLse);
-    float* delta_s = reinterpret_cast<float*>(smem + C::kOffDelta);
-    uint8_t* ds_tile = smem + C::kOffDS;
-    const float sl2 = P.scale_log2;
-    uint32_t s_phase = 0, dp_phase = 0, dse_phase = 0, ad_phase = 0;
-    int iter = 0;
+    const uint32_t tX = tmem + lane_off + C::kColX, tY = tmem + lane_off + C::kColY;
+    const float* ls_base = reinterpret_cast<const float*>(smem + C::kOffLs);
+    uint8_t* ds_row = smem + C::kOffDS + wg * kSubBytes + row * 128;
+    const uint64_t sl2x2 = f2(P.scale_log2, P.scale_log2);
+    uint32_t s_phase = 0, dp_phase = 0, ad_phase = 0;
+    int t = 0;
     for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
       const BwdItem it = decode_bwd(P, w);
       const BwdWalk wk = bwd_walk(P, it);
@@ -326,153 +452,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int b = wk.b0 + row;
       const bool validk = b < wk.L;
       const size_t krow = static_cast<size_t>(sd.row_off + it.j * P.shard_stride + b);
+      const size_t out_off = (krow * P.hkv + it.hk) * DH;
       if (wk.N == 0) {
-        if (validk) {
-          uint32_t z[32];
+        if constexpr (!kAccum) {
+          if (validk) {
+            uint32_t z[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(wg == 0 ? dk_out : dv_out) + out_off;
 #pragma unroll
-          for (int c = 0; c < DH / 32; ++c) {
-            store_row32_bf16(dk + (krow * P.hkv + it.hk) * DH + c * 32, z, 0.f);
-            store_row32_bf16(dv + (krow * P.hkv + it.hk) * DH + c * 32, z, 0.f);
+            for (int c = 0; c < DH / 32; ++c) store_row32_bf16(dst + c * 32, z, 0.f);
           }
         }
         continue;
       }
       const int64_t pk = validk ? layout_pos(P.layout, P.D, wk.L, it.j, b) : 0;
-      const bool ok = for_each_qtile(P, it, wk, [&](int r, int h, int q0) -> bool {
-        // lse (log2 domain) and delta of the query tile, double-buffered in smem
-        float* ls = lse_s + (iter & 1) * 128;
-        float* dl = delta_s + (iter & 1) * 128;
-        {
-          const int a = q0 + row;
-          if (a < wk.L) {
-            const size_t li = sd.lse_off + static_cast<size_t>(h) * P.lse_hstride +
-                              static_cast<size_t>(r) * P.shard_stride + a;
-            ls[row] = lse[li] * kLog2e;
-            dl[row] = delta[li];
-          } else {
-            ls[row] = INFINITY;  // rows beyond the piece: P = 0
-            dl[row] = 0.f;
-          }
-        }
-        // every thread of the warpgroup staged its value (bounded wait, no hang on abort)
-        mbar_arrive(&sh.lse_bar[iter & 1]);
-        if (!mbar_wait(&sh.lse_bar[iter & 1], (iter >> 1) & 1, abort_flag, tmo, status)) return false;
-        ++iter;
-        int lo = validk ? (P.causal ? first_query(P.layout, P.D, wk.L, r, pk) - q0 : 0) : 128;
-        int hi = wk.L - q0;
-        if (lo < 0) lo = 0;
-        // P^T = 2^(S^T * scale * log2e - lse * log2e), masked; bf16 pairs over S columns
+      const bool ok = for_each_qtile(P, it, wk, [&](int r, int, int q0) -> bool {
+        const int slot = t & 1;
+        const int lo = validk ? (P.causal ? first_query(P.layout, P.D, wk.L, r, pk) - q0 : 0) : 128;
+        if (!mbar_wait(&sh.ls_full[slot], (t >> 1) & 1, abort_flag, tmo, status)) return false;
+        const float* nl = ls_base + slot * 256;
+        const float* dl = nl + 128;
+        // P^T into X (bf16), kept in registers for dS^T
         if (!mbar_wait(&sh.s_full, s_phase, abort_flag, tmo, status)) return false;
         s_phase ^= 1;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32], pk16[16];
-          tmem_ld32(tS + c * 32, rr);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c * 32 + 2 * i;
-            const float p0 = (col >= lo && col < hi) ? ex2(fmaf(__uint_as_float(rr[2 * i]), sl2, -ls[col])) : 0.f;
-            const float p1 = (col + 1 >= lo && col + 1 < hi) ? ex2(fmaf(__uint_as_float(rr[2 * i + 1]), sl2, -ls[col + 1])) : 0.f;
-            pk16[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + c * 16, pk16);
+        uint32_t pp[32];
+        if (wg == 0) {
+          p_chunk<1>(tX, c0, nl, sl2x2, lo, pp);
+          p_chunk<0>(tX, c0, nl, sl2x2, lo, pp);
+        } else {
+          p_chunk<0>(tX, c0, nl, sl2x2, lo, pp);
+          p_chunk<1>(tX, c0, nl, sl2x2, lo, pp);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sh.p_full);
-        // dS^T = P^T * (dP^T - delta) -> bf16, 128B-swizzled K-major tile [K/V row][query]
+        // dS^T = P^T * (dP^T - delta). Each chunk's output lands on dP^T columns this thread
+        // has already read, so the chunk order differs between the two warpgroups.
         if (!mbar_wait(&sh.dp_full, dp_phase, abort_flag, tmo, status)) return false;
         dp_phase ^= 1;
-        if (!mbar_wait(&sh.ds_empty, dse_phase ^ 1, abort_flag, tmo, status)) return false;
-        dse_phase ^= 1;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t dp[32], pp[16];
-          tmem_ld32(tDP + c * 32, dp);
-          tmem_ld16(tS + c * 16, pp);
-          uint32_t o[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c * 32 + 2 * i;
-            const __nv_bfloat162 pv = *reinterpret_cast<const __nv_bfloat162*>(&pp[i]);
-            const float d0 = __low2float(pv) * (__uint_as_float(dp[2 * i]) - dl[col]);
-            const float d1 = __high2float(pv) * (__uint_as_float(dp[2 * i + 1]) - dl[col + 1]);
-            o[i] = pack_bf16x2(d0, d1);
-          }
-          // columns c*32 .. c*32+31 = four 16-byte chunks of sub-tile (c >> 1)
-          uint8_t* rowp = ds_tile + (c >> 1) * kSubBytes + row * 128;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int chunk = (c & 1) * 4 + q;
-            uint4 v;
-            v.x = o[4 * q + 0];
-            v.y = o[4 * q + 1];
-            v.z = o[4 * q + 2];
-            v.w = o[4 * q + 3];
-            *reinterpret_cast<uint4*>(rowp + ((chunk ^ (row & 7)) << 4)) = v;
-          }
+        if (wg == 0) {
+          ds_chunk<1, kWithDQ>(tY, c0, dl, pp, ds_row, row);
+          ds_chunk<0, kWithDQ>(tY, c0, dl, pp, ds_row, row);
+        } else {
+          ds_chunk<0, kWithDQ>(tY, c0, dl, pp, ds_row, row);
+          ds_chunk<1, kWithDQ>(tY, c0, dl, pp, ds_row, row);
         }
-        fence_proxy_async_smem();
+        mbar_arrive(&sh.ls_empty[slot]);
+        ++t;
+        tmem_st_wait();
+        if constexpr (kWithDQ) fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sh.ds_full);
         return true;
       });
       if (!ok) break;
-      // dK (times scale) and dV of this tile
+      // dK (times scale; warpgroup 0) and dV (warpgroup 1) of this tile
       if (!mbar_wait(&sh.acc_done, ad_phase, abort_flag, tmo, status)) break;
       ad_phase ^= 1;
       tc_fence_after();
+      const uint32_t tacc = tmem + lane_off + (wg == 0 ? C::kColDK : C::kColDV);
+      const float mul = wg == 0 ? P.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < DH / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(tDK + c * 32, rr);
-        if (validk) store_row32_bf16(dk + (krow * P.hkv + it.hk) * DH + c * 32, rr, P.scale);
-        tmem_ld32(tDV + c * 32, rr);
-        if (validk) store_row32_bf16(dv + (krow * P.hkv + it.hk) * DH + c * 32, rr, 1.f);
+        tmem_ld32(tacc + c * 32, rr);
+        if (validk) {
+          if constexpr (kAccum)
+            add_row32_f32(static_cast<float*>(wg == 0 ? dk_out : dv_out) + out_off + c * 32, rr, mul);
+          else
+            store_row32_bf16(static_cast<__nv_bfloat16*>(wg == 0 ? dk_out : dv_out) + out_off + c * 32,
+                             rr, mul);
+        }
       }
       tc_fence_before();
-      mbar_arrive(&sh.acc_free);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------------ dQ warpgroup
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
-    const uint32_t tDQ = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
-    uint32_t dqf_phase = 0;
-    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
-      const BwdItem it = decode_bwd(P, w);
-      const BwdWalk wk = bwd_walk(P, it);
-      if (wk.N == 0) continue;
-      const SeqDesc& sd = P.seq[it.seq];
-      const bool ok = for_each_qtile(P, it, wk, [&](int r, int h, int q0) -> bool {
-        if (!mbar_wait(&sh.dq_full, dqf_phase, abort_flag, tmo, status)) return false;
-        dqf_phase ^= 1;
-        tc_fence_after();
-        const int a = q0 + row;
-        const bool valid = a < wk.L;
-        float4* dst = reinterpret_cast<float4*>(
-            dq_acc + (static_cast<size_t>(sd.row_off + r * P.shard_stride + a) * P.hq + h) * DH);
+    if constexpr (kWithDQ) {
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
+      const uint32_t tQ = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColY;
+      const float mul = P.dq_mul;
+      uint32_t dqf_phase = 0;
+      for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+        const BwdItem it = decode_bwd(P, w);
+        const BwdWalk wk = bwd_walk(P, it);
+        if (wk.N == 0) continue;
+        const SeqDesc& sd = P.seq[it.seq];
+        const bool ok = for_each_qtile(P, it, wk, [&](int r, int h, int q0) -> bool {
+          if (!mbar_wait(&sh.dq_full, dqf_phase, abort_flag, tmo, status)) return false;
+          dqf_phase ^= 1;
+          tc_fence_after();
+          const int a = q0 + row;
+          const bool valid = a < wk.L;
+          float* dst =
+              dq_acc + (static_cast<size_t>(sd.row_off + r * P.shard_stride + a) * P.hq + h) * DH;
 #pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(tDQ + c * 32, rr);
-          if (valid) {
+          for (int c = 0; c < DH / 32; ++c) {
+            uint32_t rr[32];
+            tmem_ld32(tQ + c * 32, rr);
+            if (c == DH / 32 - 1) {  // every column of Y has been read: release it
+              tc_fence_before();
+              mbar_arrive(&sh.dq_free);
+            }
+            if (valid) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              atomicAdd(dst + c * 8 + q,
-                        make_float4(__uint_as_float(rr[4 * q]), __uint_as_float(rr[4 * q + 1]),
-                                    __uint_as_float(rr[4 * q + 2]), __uint_as_float(rr[4 * q + 3])));
+              for (int q = 0; q < 8; ++q)
+                red_add_v4(dst + c * 32 + 4 * q, __uint_as_float(rr[4 * q]) * mul,
+                           __uint_as_float(rr[4 * q + 1]) * mul, __uint_as_float(rr[4 * q + 2]) * mul,
+                           __uint_as_float(rr[4 * q + 3]) * mul);
+            }
           }
-        }
-        tc_fence_before();
-        mbar_arrive(&sh.dq_free);
-        return true;
-      });
-      if (!ok) break;
+          return true;
+        });
+        if (!ok) break;
+      }
     }
   }
 
@@ -484,26 +581,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-template <int DH>
+template <int DH, bool kWithDQ, bool kAccum>
 cudaError_t launch_one(const Plan& P, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, const float* lse,
                        const float* delta, float* dq_acc, void* dk, void* dv, int n_sm,
                        cudaStream_t st) {
   using C = BwdCfg<DH>;
-  auto kern = ring_bwd_tc_kernel<DH>;
+  auto kern = ring_bwd_tc_kernel<DH, kWithDQ, kAccum>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = P.n_items < n_sm ? P.n_items : n_sm;
-  kern<<<grid, kBwdThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta, dq_acc,
-                                                 static_cast<__nv_bfloat16*>(dk),
-                                                 static_cast<__nv_bfloat16*>(dv));
+  kern<<<grid, kBwdThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta, dq_acc, dk, dv);
   return cudaGetLastError();
+}
+
+template <bool kWithDQ, bool kAccum>
+cudaError_t launch_dh(const Plan& P, const CUtensorMap& mq, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const float* lse,
+                      const float* delta, float* dq_acc, void* dk, void* dv, int n_sm,
+                      cudaStream_t st) {
+  if (P.head_dim == 128)
+    return launch_one<128, kWithDQ, kAccum>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+  return launch_one<64, kWithDQ, kAccum>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const Plan& P, const void* q, const void* k, const void* v,
+cudaError_t launch_bwd_tc(const Plan& P, BwdKind kind, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse, const float* delta, float* dq_acc,
                           void* dk, void* dv, cudaStream_t st) {
   if (P.n_items == 0) return cudaSuccess;
@@ -516,9 +621,15 @@ cudaError_t launch_bwd_tc(const Plan& P, const void* q, const void* k, const voi
   int dev = 0, n_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  if (P.head_dim == 128)
-    return launch_one<128>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
-  return launch_one<64>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+  switch (kind) {
+    case BwdKind::kFused:
+      return launch_dh<true, false>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+    case BwdKind::kKvOnly:
+      return launch_dh<false, false>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+    case BwdKind::kBlockAccum:
+      return launch_dh<true, true>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t bwd_status(unsigned int* value, bool reset) {

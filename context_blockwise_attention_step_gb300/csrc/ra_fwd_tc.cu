@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
     const float sl2 = P.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
     uint32_t s_phase = 0, od_phase = 0;
     for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
       const FwdItem it = decode_fwd(P, w);
@@ -321,15 +322,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tc_fence_after();
           int cnt = lim + 1 - b * kKvTileRows;
           cnt = cnt < 0 ? 0 : (cnt > kKvTileRows ? kKvTileRows : cnt);
+          const bool full = __all_sync(0xffffffffu, cnt == kKvTileRows);  // no mask needed
           // pass 1: row max over the visible columns
           float mx = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
             tmem_ld32(tS + c * 32, r);
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              mx = fmaxf(mx, (c * 32 + i < cnt) ? __uint_as_float(r[i]) : -INFINITY);
+              for (int i = 0; i < 16; ++i)
+                mx = max3(mx, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                mx = fmaxf(mx, (c * 32 + i < cnt) ? __uint_as_float(r[i]) : -INFINITY);
+            }
           }
           mx *= sl2;
           const float m_new = fmaxf(m, mx);
@@ -349,20 +357,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           if (grow) m = m_new;
           const float mref = (m == -INFINITY) ? 0.f : m;
-          // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs over the consumed S columns
+          // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs over the consumed S columns.
+          // Three pairs in eight take 2^x from the FMA pipe (exp2_poly2), the rest from the
+          // MUFU unit, so that neither unit limits the tile rate.
+          const uint64_t nm2 = f2(-mref, -mref);
+          uint64_t l2 = f2(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32], pk[16];
             tmem_ld32(tS + c * 32, r);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int col = c * 32 + 2 * i;
-              const float p0 = (col < cnt) ? ex2(fmaf(__uint_as_float(r[2 * i]), sl2, -mref)) : 0.f;
-              const float p1 = (col + 1 < cnt) ? ex2(fmaf(__uint_as_float(r[2 * i + 1]), sl2, -mref)) : 0.f;
-              l += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
+              const uint64_t x = fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, nm2);
+              uint64_t p2;
+              if ((i & 7) < 3) {
+                p2 = exp2_poly2(x);
+              } else {
+                const float2 e = f2_split(x);
+                p2 = f2(ex2(e.x), ex2(e.y));
+              }
+              if (!full) {
+                const int col = c * 32 + 2 * i;
+                float2 pv = f2_split(p2);
+                if (col >= cnt) pv.x = 0.f;
+                if (col + 1 >= cnt) pv.y = 0.f;
+                p2 = f2(pv.x, pv.y);
+              }
+              l2 = add2(l2, p2);
+              pk[i] = bf16x2_of(p2);
             }
             tmem_st16(tS + c * 16, pk);
+          }
+          {
+            const float2 ls = f2_split(l2);
+            l += ls.x + ls.y;
           }
           tmem_st_wait();
           tc_fence_before();
@@ -412,6 +440,16 @@ __global__ void wait_timeout_kernel(uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// exp2_poly2 on n values (test hook for its error bound).
+__global__ void exp2_poly_kernel(const float* __restrict__ x, float* __restrict__ y, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x1 = i + 1 < n ? x[i + 1] : 0.f;
+  const float2 r = f2_split(exp2_poly2(f2(x[i], x1)));
+  y[i] = r.x;
+  if (i + 1 < n) y[i + 1] = r.y;
+}
+
 template <int DH, typename OutT>
 cudaError_t launch_one(const Plan& P, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, OutT* out, float* lse, int n_sm, cudaStream_t st) {
@@ -444,6 +482,12 @@ cudaError_t launch_fwd_tc(const Plan& P, const void* q, const void* k, const voi
   }
   return P.out_f32 ? launch_one<64, float>(P, mq, mk, mv, static_cast<float*>(out), lse, n_sm, st)
                    : launch_one<64, __nv_bfloat16>(P, mq, mk, mv, static_cast<__nv_bfloat16*>(out), lse, n_sm, st);
+}
+
+cudaError_t launch_exp2_poly(const float* x, float* y, int n, cudaStream_t st) {
+  const int pairs = (n + 1) / 2;
+  exp2_poly_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(x, y, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_timeout(uint64_t timeout_ns, cudaStream_t st) {

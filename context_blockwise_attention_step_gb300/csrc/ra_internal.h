@@ -19,10 +19,21 @@ cudaError_t make_token_tmap(CUtensorMap* map, const void* base, int rows, int he
 // Tensor-core (bf16, head_dim 64/128) kernels.
 cudaError_t launch_fwd_tc(const Plan& P, const void* q, const void* k, const void* v, void* out,
                           float* lse, cudaStream_t st);
-cudaError_t launch_bwd_tc(const Plan& P, const void* q, const void* k, const void* v,
+// Backward K/V-tile kernel variants: kFused (dq sums into dq_acc, dk / dv stored in the
+// problem dtype), kKvOnly (dk / dv only; dq_acc unused), kBlockAccum (float32 dq, dk, dv
+// added into the outputs).
+enum class BwdKind { kFused, kKvOnly, kBlockAccum };
+cudaError_t launch_bwd_tc(const Plan& P, BwdKind kind, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse, const float* delta, float* dq_acc,
                           void* dk, void* dv, cudaStream_t st);
+// Query-tile-major dq of the deterministic backward (bf16, head_dim 64/128): dq written in
+// the problem dtype, no atomics. The plan's items are re-numbered inside.
+cudaError_t launch_bwd_dq_tc(const Plan& P, const void* q, const void* k, const void* v,
+                             const void* dout, const float* lse, const float* delta, void* dq,
+                             cudaStream_t st);
+cudaError_t bwd_dq_status(unsigned int* value, bool reset);
 cudaError_t launch_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_exp2_poly(const float* x, float* y, int n, cudaStream_t st);
 cudaError_t fwd_status(unsigned int* value, bool reset);
 cudaError_t bwd_status(unsigned int* value, bool reset);
 

@@ -33,24 +33,31 @@ long max_len(const Plan& P) {
 
 // ------------------------------------------------------------------ update_out_and_lse
 // lse' = log(e^lse + e^blse); out' = e^(lse-lse') out + e^(blse-lse') bout; -inf identity.
-// One thread per 4 consecutive elements of a (row, head) (VEC = 4) or per element.
+// One warp per (row, head): lane 0 reads both lse values and broadcasts them, the lanes
+// walk the row in VEC-element pieces (VEC = 4 when head_dim % 4 == 0), and lane 0 writes
+// the merged lse only after the broadcast, so no lane can read an already-merged lse.
 template <typename BT, int VEC>
 __global__ void __launch_bounds__(kThreads)
     merge_kernel(const __grid_constant__ Plan P, float* __restrict__ out, float* __restrict__ lse,
                  const BT* __restrict__ bout, const float* __restrict__ blse) {
   const SeqDesc& sd = P.seq[blockIdx.y];
-  const int L = sd.L, dh = P.head_dim, nv = dh / VEC;
-  const long units = static_cast<long>(plan_ranks(P)) * L * P.hq * nv;
-  for (long u = static_cast<long>(blockIdx.x) * kThreads + threadIdx.x; u < units;
-       u += static_cast<long>(gridDim.x) * kThreads) {
-    const int c = static_cast<int>(u % nv);
-    long x = u / nv;
-    const int h = static_cast<int>(x % P.hq);
-    x /= P.hq;
+  const int L = sd.L, dh = P.head_dim, nv = dh / VEC, lane = threadIdx.x & 31;
+  const long units = static_cast<long>(plan_ranks(P)) * L * P.hq;
+  constexpr int kWarps = kThreads / 32;
+  for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < units;
+       u += static_cast<long>(gridDim.x) * kWarps) {
+    const int h = static_cast<int>(u % P.hq);
+    const long x = u / P.hq;
     const int a = static_cast<int>(x % L);
     const int r = P.rank_only >= 0 ? P.rank_only : static_cast<int>(x / L);
     const size_t li = lse_index(P, sd, h, r, a);
-    const float l1 = lse[li], l2 = blse[li];
+    float l1 = 0.f, l2 = 0.f;
+    if (lane == 0) {
+      l1 = lse[li];
+      l2 = blse[li];
+    }
+    l1 = __shfl_sync(0xffffffffu, l1, 0);
+    l2 = __shfl_sync(0xffffffffu, l2, 0);
     const float mx = fmaxf(l1, l2);
     float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
     if (mx != -INFINITY) {
@@ -61,8 +68,10 @@ __global__ void __launch_bounds__(kThreads)
       w2 = e2 / s;
     }
     const size_t row = static_cast<size_t>(sd.row_off + r * P.shard_stride + a);
-    const size_t e0 = (row * P.hq + h) * dh + static_cast<size_t>(c) * VEC;
-    if (mx != -INFINITY) {
+    if (lane == 0) lse[li] = lnew;
+    if (mx == -INFINITY) continue;
+    for (int c = lane; c < nv; c += 32) {
+      const size_t e0 = (row * P.hq + h) * dh + static_cast<size_t>(c) * VEC;
       if constexpr (VEC == 4) {
         float4 o = *reinterpret_cast<float4*>(out + e0);
         float b[4];
@@ -85,7 +94,6 @@ __global__ void __launch_bounds__(kThreads)
         out[e0] = w1 * out[e0] + w2 * ldf(bout + e0);
       }
     }
-    if (c == 0) lse[li] = lnew;
   }
 }
 
@@ -97,13 +105,13 @@ __global__ void __launch_bounds__(kThreads)
                  float* __restrict__ delta) {
   const SeqDesc& sd = P.seq[blockIdx.y];
   const int L = sd.L, dh = P.head_dim, lane = threadIdx.x & 31;
-  const long units = static_cast<long>(P.D) * L * P.hq;
+  const long units = static_cast<long>(plan_ranks(P)) * L * P.hq;
   constexpr int kWarps = kThreads / 32;
   for (long u = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < units;
        u += static_cast<long>(gridDim.x) * kWarps) {
     const int h = static_cast<int>(u % P.hq);
     const int a = static_cast<int>((u / P.hq) % L);
-    const int r = static_cast<int>(u / (static_cast<long>(P.hq) * L));
+    const int r = P.rank_only >= 0 ? P.rank_only : static_cast<int>(u / (static_cast<long>(P.hq) * L));
     const size_t base = (static_cast<size_t>(sd.row_off + r * P.shard_stride + a) * P.hq + h) * dh;
     float s = 0.f;
     for (int d = lane; d < dh; d += 32) s += ldf(o + base + d) * ldf(dout + base + d);
@@ -114,6 +122,7 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------------ backward postprocess
+// dq = bf16(dq sums); the tensor-core kernel already applied the softmax scale.
 __global__ void __launch_bounds__(kThreads)
     dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq, long n4, float scale) {
   for (long i = static_cast<long>(blockIdx.x) * kThreads + threadIdx.x; i < n4;
@@ -172,8 +181,8 @@ __global__ void __launch_bounds__(kThreads)
 cudaError_t launch_merge(const Plan& P, float* out, float* lse, const void* block_out,
                          int block_f32, const float* block_lse, cudaStream_t st) {
   const int vec = P.head_dim % 4 == 0 ? 4 : 1;
-  const long work = plan_ranks(P) * max_len(P) * P.hq * (P.head_dim / vec);
-  const dim3 grid(grid_for(work, kThreads), P.n_seqs);
+  const long work = plan_ranks(P) * max_len(P) * P.hq;  // one warp per (row, head)
+  const dim3 grid(grid_for(work, kThreads / 32), P.n_seqs);
   if (block_f32) {
     if (vec == 4) merge_kernel<float, 4><<<grid, kThreads, 0, st>>>(P, out, lse, (const float*)block_out, block_lse);
     else merge_kernel<float, 1><<<grid, kThreads, 0, st>>>(P, out, lse, (const float*)block_out, block_lse);
@@ -186,7 +195,7 @@ cudaError_t launch_merge(const Plan& P, float* out, float* lse, const void* bloc
 
 cudaError_t launch_bwd_delta(const Plan& P, int dtype, const void* out, const void* dout,
                              float* delta, cudaStream_t st) {
-  const long work = P.D * max_len(P) * P.hq;
+  const long work = plan_ranks(P) * max_len(P) * P.hq;
   const dim3 grid(grid_for(work, kThreads / 32), P.n_seqs);
   if (dtype == RA_F32)
     delta_kernel<float><<<grid, kThreads, 0, st>>>(P, (const float*)out, (const float*)dout, delta);
@@ -198,7 +207,7 @@ cudaError_t launch_bwd_delta(const Plan& P, int dtype, const void* out, const vo
 cudaError_t launch_dq_convert(const Plan& P, const float* dq_acc, void* dq, cudaStream_t st) {
   const long n4 = static_cast<long>(P.n_rows) * P.hq * P.head_dim / 4;
   dq_convert_kernel<<<grid_for(n4, kThreads), kThreads, 0, st>>>(
-      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq), n4, P.scale);
+      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq), n4, 1.f);
   return cudaGetLastError();
 }
 

@@ -27,7 +27,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device, looked up once per device and kept
+// for the life of the process (a context torn down by cudaDeviceReset is not supported).
 cudaError_t scratch_on_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -34,10 +34,13 @@ struct Plan {
   int32_t lse_hstride;   // lse elements between heads
   int32_t n_rows;        // rows of the token axis (B*S or T)
   int32_t n_seqs, n_items;
-  int32_t step_begin, step_end;  // ring steps covered by a forward launch
+  int32_t step_begin, step_end;  // ring steps covered by a launch: [begin, end)
   int32_t rank_only;             // >= 0: only this rank's query rows (block mode)
+  int32_t kv_shard_only;         // backward, >= 0: only this K/V shard's tiles are items
   int32_t out_f32;               // forward output stored as float32 (else problem dtype)
+  int32_t bwd_accum;             // backward: add float32 gradients into the outputs
   float scale, scale_log2;
+  float dq_mul;                  // factor on dS K before it is added to the dq sums
   uint64_t timeout_ns;
   SeqDesc seq[RA_MAX_SEQS];
 };
@@ -50,9 +53,19 @@ RA_HD int plan_ranks(const Plan& P) { return P.rank_only >= 0 ? 1 : P.D; }
 RA_HD int fwd_items_of(const Plan& P, int L) {
   return ceil_div(L, kFwdBlockRows) * plan_ranks(P) * P.hq;
 }
-// Backward items of one sequence: one per (128-row K/V tile, rank, K/V head).
+RA_HD int plan_kv_shards(const Plan& P) { return P.kv_shard_only >= 0 ? 1 : P.D; }
+
+// Backward items of one sequence: one per (128-row K/V tile, K/V shard, K/V head).
 RA_HD int bwd_items_of(const Plan& P, int L) {
-  return ceil_div(L, kKvTileRows) * P.D * P.hkv;
+  return ceil_div(L, kKvTileRows) * plan_kv_shards(P) * P.hkv;
+}
+
+// Whether the backward walk of K/V shard j visits query rank r: the ring step at which
+// r holds shard j, (r - j) mod D, must lie in [step_begin, step_end), and r must be the
+// selected rank when one is selected.
+RA_HD bool rank_in_walk(const Plan& P, int j, int r) {
+  const int s = ((r - j) % P.D + P.D) % P.D;
+  return s >= P.step_begin && s < P.step_end && (P.rank_only < 0 || r == P.rank_only);
 }
 
 RA_HD int find_seq(const Plan& P, int w) {
@@ -67,20 +80,22 @@ RA_HD int find_seq(const Plan& P, int w) {
 struct FwdItem { int seq, h, r, blk; };
 struct BwdItem { int seq, hk, j, kt; };
 
-// Forward decode: the last query block first (for causal layouts it sees the most keys),
-// ranks next, query heads innermost (the heads of a GQA group then read the same K/V
-// tiles at about the same time, from L2).
+// Forward decode: K/V heads outermost, so that the CTAs running at the same time read the
+// K/V of one head (a working set that stays in L2); within a head the last query block
+// first (for causal layouts it sees the most keys), then ranks, then the query heads of
+// the GQA group (which read the same K/V tiles at about the same time).
 RA_HD FwdItem decode_fwd(const Plan& P, int w) {
   FwdItem it;
   it.seq = find_seq(P, w);
   const SeqDesc& s = P.seq[it.seq];
+  const int nblk = ceil_div(s.L, kFwdBlockRows), nr = plan_ranks(P);
   int x = w - s.item_start;
-  it.h = x % P.hq;
-  x /= P.hq;
-  const int nr = plan_ranks(P);
+  const int g = x % P.group;
+  x /= P.group;
   it.r = P.rank_only >= 0 ? P.rank_only : x % nr;
   x /= nr;
-  it.blk = ceil_div(s.L, kFwdBlockRows) - 1 - x;
+  it.blk = nblk - 1 - x % nblk;
+  it.h = (x / nblk) * P.group + g;
   return it;
 }
 
@@ -92,12 +107,13 @@ RA_HD BwdItem decode_bwd(const Plan& P, int w) {
   BwdItem it;
   it.seq = find_seq(P, w);
   const SeqDesc& s = P.seq[it.seq];
-  const int per_head = ceil_div(s.L, kKvTileRows) * P.D;
+  const int ns = plan_kv_shards(P);
+  const int per_head = ceil_div(s.L, kKvTileRows) * ns;
   int x = w - s.item_start;
   it.hk = x / per_head;
   x %= per_head;
-  it.j = x % P.D;
-  it.kt = x / P.D;
+  it.j = P.kv_shard_only >= 0 ? P.kv_shard_only : x % ns;
+  it.kt = x / ns;
   return it;
 }
 

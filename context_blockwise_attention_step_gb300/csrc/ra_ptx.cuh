@@ -224,6 +224,86 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Packed pairs of f32 in one 64-bit register (sm_100 family f32x2 arithmetic): element 0
+// in the low half. Denormal results flush to zero, like ex2.approx.ftz.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair, on the FMA pipe instead of the MUFU unit (to share the exponentials of
+// the softmax between the two units). Cody-Waite style split x = n + f with n = round(x)
+// taken from the low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f by a degree-3
+// polynomial fitted here for minimum relative error on [-1/2, 1/2] (max 7.5e-5, i.e. about
+// 1/50 of a bf16 ulp); 2^n applied by adding n to the exponent field. Needs x <= 127; x
+// is clamped below at -125 so that the result stays a normal float (2^-125 stands for 0).
+__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
+  constexpr float c0 = 0.99992806f, c1 = 0.69326097f, c2 = 0.24261113f, c3 = 0.05517167f;
+  constexpr float magic = 12582912.0f;  // 1.5 * 2^23
+  float2 v = f2_split(x);
+  v.x = fmaxf(v.x, -125.f);
+  v.y = fmaxf(v.y, -125.f);
+  const uint64_t xc = f2(v.x, v.y);
+  const uint64_t t = add2(xc, f2(magic, magic));
+  const uint64_t f = sub2(xc, sub2(t, f2(magic, magic)));
+  uint64_t p = fma2(f2(c3, c3), f, f2(c2, c2));
+  p = fma2(p, f, f2(c1, c1));
+  p = fma2(p, f, f2(c0, c0));
+  const float2 pf = f2_split(p), tf = f2_split(t);
+  return f2(__uint_as_float(__float_as_uint(pf.x) + (__float_as_uint(tf.x) << 23)),
+            __uint_as_float(__float_as_uint(pf.y) + (__float_as_uint(tf.y) << 23)));
+}
+
+// Round a packed f32 pair to a bf16 pair (low element in the low half).
+__device__ __forceinline__ uint32_t bf16x2_of(uint64_t v) {
+  const float2 f = f2_split(v);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
+  return r;
+}
+// Widen a bf16 pair to a packed f32 pair (exact).
+__device__ __forceinline__ uint64_t f2_of_bf16x2(uint32_t v) {
+  return f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// Fire-and-forget vector reduction into global memory (four f32 adds, 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // Named barrier over `count` threads (multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -117,20 +117,22 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 }
 
 // -------------------------------------------------------------------------------- backward
-template <typename T>
+// Block mode (the unfused path's per-step backward): only the steps [step_begin, step_end)
+// and, if set, the rank rank_only; OutT = float with kAccum adds into the outputs.
+template <typename T, typename OutT, bool kAccum>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     bwd_dq_simt_kernel(const __grid_constant__ Plan P, const T* __restrict__ q,
                        const T* __restrict__ k, const T* __restrict__ v,
                        const T* __restrict__ dout, const float* __restrict__ lse,
-                       const float* __restrict__ delta, T* __restrict__ dq) {
+                       const float* __restrict__ delta, OutT* __restrict__ dq) {
   const SeqDesc& sd = P.seq[blockIdx.y];
   const int L = sd.L, dh = P.head_dim, lane = threadIdx.x & 31;
-  const long units = static_cast<long>(P.D) * L * P.hq;
+  const long units = static_cast<long>(plan_ranks(P)) * L * P.hq;
   for (long u = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); u < units;
        u += static_cast<long>(gridDim.x) * kWarpsPerBlock) {
     const int h = static_cast<int>(u % P.hq);
     const int a = static_cast<int>((u / P.hq) % L);
-    const int r = static_cast<int>(u / (static_cast<long>(P.hq) * L));
+    const int r = P.rank_only >= 0 ? P.rank_only : static_cast<int>(u / (static_cast<long>(P.hq) * L));
     const int hk = h / P.group;
     const int qrow = sd.row_off + r * P.shard_stride + a;
     const size_t li = sd.lse_off + static_cast<size_t>(h) * P.lse_hstride + static_cast<size_t>(r) * P.shard_stride + a;
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
     const int64_t pq = layout_pos(P.layout, P.D, L, r, a);
-    for (int s = 0; s < P.D; ++s) {
+    for (int s = P.step_begin; s < P.step_end; ++s) {
       const int j = shard_at_step(P.D, r, s);
       const int lim = P.causal ? key_limit(P.layout, P.D, L, j, pq) : L - 1;
       for (int b = 0; b <= lim; ++b) {
@@ -157,29 +159,32 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         }
       }
     }
-    T* o = dq + (static_cast<size_t>(qrow) * P.hq + h) * dh;
+    OutT* o = dq + (static_cast<size_t>(qrow) * P.hq + h) * dh;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int d = lane + 32 * i;
-      if (d < dh) st<T>(o + d, acc[i] * P.scale);
+      if (d < dh) {
+        if constexpr (kAccum) o[d] += acc[i] * P.scale;
+        else st<OutT>(o + d, acc[i] * P.scale);
+      }
     }
   }
 }
 
-template <typename T>
+template <typename T, typename OutT, bool kAccum>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     bwd_dkv_simt_kernel(const __grid_constant__ Plan P, const T* __restrict__ q,
                         const T* __restrict__ k, const T* __restrict__ v,
                         const T* __restrict__ dout, const float* __restrict__ lse,
-                        const float* __restrict__ delta, T* __restrict__ dk, T* __restrict__ dv) {
+                        const float* __restrict__ delta, OutT* __restrict__ dk, OutT* __restrict__ dv) {
   const SeqDesc& sd = P.seq[blockIdx.y];
   const int L = sd.L, dh = P.head_dim, lane = threadIdx.x & 31;
-  const long units = static_cast<long>(P.D) * L * P.hkv;
+  const long units = static_cast<long>(plan_kv_shards(P)) * L * P.hkv;
   for (long u = static_cast<long>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5); u < units;
        u += static_cast<long>(gridDim.x) * kWarpsPerBlock) {
     const int hk = static_cast<int>(u % P.hkv);
     const int b = static_cast<int>((u / P.hkv) % L);
-    const int j = static_cast<int>(u / (static_cast<long>(P.hkv) * L));
+    const int j = P.kv_shard_only >= 0 ? P.kv_shard_only : static_cast<int>(u / (static_cast<long>(P.hkv) * L));
     const size_t krow = static_cast<size_t>(sd.row_off + j * P.shard_stride + b);
     float kr[kMaxPerLane], vr[kMaxPerLane], dka[kMaxPerLane], dva[kMaxPerLane];
     load_row(k + (krow * P.hkv + hk) * dh, dh, lane, kr);
@@ -189,8 +194,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     const int64_t pk = layout_pos(P.layout, P.D, L, j, b);
     for (int g = 0; g < P.group; ++g) {
       const int h = hk * P.group + g;
-      for (int s = 0; s < P.D; ++s) {
+      for (int s = P.step_begin; s < P.step_end; ++s) {
         const int r = rank_at_step(P.D, j, s);
+        if (P.rank_only >= 0 && r != P.rank_only) continue;
         const int a_begin = P.causal ? first_query(P.layout, P.D, L, r, pk) : 0;
         for (int a = a_begin; a < L; ++a) {
           const size_t qrow = static_cast<size_t>(sd.row_off + r * P.shard_stride + a);
@@ -215,8 +221,13 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int d = lane + 32 * i;
       if (d < dh) {
-        st<T>(dk + (krow * P.hkv + hk) * dh + d, dka[i] * P.scale);
-        st<T>(dv + (krow * P.hkv + hk) * dh + d, dva[i]);
+        if constexpr (kAccum) {
+          dk[(krow * P.hkv + hk) * dh + d] += dka[i] * P.scale;
+          dv[(krow * P.hkv + hk) * dh + d] += dva[i];
+        } else {
+          st<OutT>(dk + (krow * P.hkv + hk) * dh + d, dka[i] * P.scale);
+          st<OutT>(dv + (krow * P.hkv + hk) * dh + d, dva[i]);
+        }
       }
     }
   }
@@ -260,21 +271,35 @@ cudaError_t launch_fwd_simt(const Plan& P, int dtype, const void* q, const void*
 cudaError_t launch_bwd_simt(const Plan& P, int dtype, const void* q, const void* k,
                             const void* v, const void* dout, const float* lse,
                             const float* delta, void* dq, void* dk, void* dv, cudaStream_t st) {
-  const dim3 gq = seq_grid(P, P.D * max_len(P) * P.hq);
-  const dim3 gk = seq_grid(P, P.D * max_len(P) * P.hkv);
+  const dim3 gq = seq_grid(P, plan_ranks(P) * max_len(P) * P.hq);
+  const dim3 gk = seq_grid(P, plan_kv_shards(P) * max_len(P) * P.hkv);
   const dim3 block(32 * kWarpsPerBlock);
-  if (dtype == RA_F32) {
+  if (P.bwd_accum) {
+    if (dtype == RA_F32) {
+      using T = float;
+      bwd_dq_simt_kernel<T, float, true><<<gq, block, 0, st>>>(
+          P, (const T*)q, (const T*)k, (const T*)v, (const T*)dout, lse, delta, (float*)dq);
+      bwd_dkv_simt_kernel<T, float, true><<<gk, block, 0, st>>>(
+          P, (const T*)q, (const T*)k, (const T*)v, (const T*)dout, lse, delta, (float*)dk, (float*)dv);
+    } else {
+      using T = __nv_bfloat16;
+      bwd_dq_simt_kernel<T, float, true><<<gq, block, 0, st>>>(
+          P, (const T*)q, (const T*)k, (const T*)v, (const T*)dout, lse, delta, (float*)dq);
+      bwd_dkv_simt_kernel<T, float, true><<<gk, block, 0, st>>>(
+          P, (const T*)q, (const T*)k, (const T*)v, (const T*)dout, lse, delta, (float*)dk, (float*)dv);
+    }
+  } else if (dtype == RA_F32) {
     using T = float;
-    bwd_dq_simt_kernel<T><<<gq, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
-                                                 (const T*)dout, lse, delta, (T*)dq);
-    bwd_dkv_simt_kernel<T><<<gk, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
-                                                  (const T*)dout, lse, delta, (T*)dk, (T*)dv);
+    bwd_dq_simt_kernel<T, T, false><<<gq, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
+                                                           (const T*)dout, lse, delta, (T*)dq);
+    bwd_dkv_simt_kernel<T, T, false><<<gk, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
+                                                            (const T*)dout, lse, delta, (T*)dk, (T*)dv);
   } else {
     using T = __nv_bfloat16;
-    bwd_dq_simt_kernel<T><<<gq, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
-                                                 (const T*)dout, lse, delta, (T*)dq);
-    bwd_dkv_simt_kernel<T><<<gk, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
-                                                  (const T*)dout, lse, delta, (T*)dk, (T*)dv);
+    bwd_dq_simt_kernel<T, T, false><<<gq, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
+                                                           (const T*)dout, lse, delta, (T*)dq);
+    bwd_dkv_simt_kernel<T, T, false><<<gk, block, 0, st>>>(P, (const T*)q, (const T*)k, (const T*)v,
+                                                            (const T*)dout, lse, delta, (T*)dk, (T*)dv);
   }
   return cudaGetLastError();
 }

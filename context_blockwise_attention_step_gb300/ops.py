@@ -173,6 +173,26 @@ def ring_attn_bwd(dout, q, k, v, out, lse, prob: Problem, dq=None, dk=None, dv=N
     return dq, dk, dv
 
 
+def block_attn_bwd(dout, q, k, v, out, lse, prob: Problem, rank: int, step: int, dq_acc, dk_acc,
+                   dv_acc, workspace=None, stream=None):
+    """One ring step of the unfused backward: adds the float32 block gradients of ``rank``
+    (every rank if -1) at ``step`` into ``dq_acc`` (rank's rows) and ``dk_acc`` / ``dv_acc``
+    (rows of shard (rank - step) mod D)."""
+    r = prob.raw
+    nq, nk = prob.rows * r.hq * r.head_dim, prob.rows * r.hkv * r.head_dim
+    for t, n, name in ((dout, nq, "dout"), (q, nq, "q"), (k, nk, "k"), (v, nk, "v"), (out, nq, "out")):
+        _check_tensor(t, prob.token_dtype, n, name)
+    _check_tensor(lse, torch.float32, prob.rows * r.hq, "lse")
+    for t, n, name in ((dq_acc, nq, "dq_acc"), (dk_acc, nk, "dk_acc"), (dv_acc, nk, "dv_acc")):
+        _check_tensor(t, torch.float32, n, name)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_bytes(prob, 2), 1), device=q.device, dtype=torch.uint8)
+    check(lib().ra_block_attn_bwd(prob.ptr, rank, step, _p(q), _p(k), _p(v), _p(out), _p(lse),
+                                  _p(dout), _p(dq_acc), _p(dk_acc), _p(dv_acc), _p(workspace),
+                                  workspace.numel(), _stream(stream)))
+    return dq_acc, dk_acc, dv_acc
+
+
 def ring_attn_bwd_noalloc(dout, q, k, v, out, lse, prob: Problem, dq, dk, dv, stream=None):
     """ring_attn_bwd without a caller workspace, for callers that cannot allocate device
     memory: the library's static scratch array is used (problems up to

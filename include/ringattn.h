@@ -120,8 +120,9 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
                           const void* block_out, int block_out_dtype, const float* block_lse,
                           void* stream);
 
-/* Bytes of device workspace ra_ring_attn_bwd needs (which = 1). which = 0 (forward) is 0.
- * Returns 0 for an invalid problem as well; call ra_validate to tell the two apart. */
+/* Bytes of device workspace: which = 1 for ra_ring_attn_bwd, which = 2 for
+ * ra_block_attn_bwd; which = 0 (forward) is 0. Returns 0 for an invalid problem as well;
+ * call ra_validate to tell the two apart. */
 size_t ra_workspace_bytes(const ra_problem* p, int which);
 
 /* Ring backward (how-to page, "Backward Pass and Gradient Accumulation"): the blocks of
@@ -137,6 +138,23 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* One ring step of the unfused backward (how-to page, "Backward Pass and Gradient
+ * Accumulation": per step, the block is differentiated against the FINAL out and lse, then
+ * dq += block_dq on the rank and block_dk / block_dv are added into the K/V shard's
+ * gradients). Rank `rank` (every rank if rank < 0) at step `step` holds K/V shard
+ * (rank - step) mod D; this call ADDS, in float32:
+ *   dq_acc rows of rank `rank`                     += block_dq   (layout like q)
+ *   dk_acc, dv_acc rows of shard (rank-step) mod D += block_dk, block_dv (layout like k)
+ * Summing the calls of steps 0..D-1 into zeroed accumulators gives the full backward.
+ * Inputs as for ra_ring_attn_bwd (out, lse: the final forward results). The workspace
+ * (device, >= ra_workspace_bytes(p, 2), 256-byte aligned) receives the per-row
+ * dot(dout, out) of the selected rank(s); it is overwritten. Rows outside the selection are
+ * not touched. Calls must not overlap on the GPU when they add into the same rows. */
+int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, const void* k,
+                      const void* v, const void* out, const float* lse, const void* dout,
+                      float* dq_acc, float* dk_acc, float* dv_acc, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
 /* The same backward for callers that cannot allocate device memory (a plain-C plugin
  * handed only its input and output buffers, or a caller that must keep cudaMalloc and its
  * device-wide synchronisation out of a training step). The pages have no counterpart: on
@@ -146,7 +164,9 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
  * Arguments as for ra_ring_attn_bwd minus the workspace. Problems whose
  * ra_workspace_bytes(p, 1) exceeds the array are rejected with RA_ERR_WORKSPACE and nothing
  * is launched. The first call on a device looks the array's address up on that device
- * (make that first call before any stream capture). Every call shares the array and the
+ * and keeps it for the life of the process (make that first call before any stream
+ * capture; a cudaDeviceReset after it is not supported, since the kept address would then
+ * be stale). Every call shares the array and the
  * backward clears what must start at zero, but calls that overlap on the GPU race on it:
  * order them on one stream. Allocates nothing. */
 #define RA_NOALLOC_SCRATCH_BYTES (64u << 20)
@@ -198,6 +218,12 @@ int ra_check_device_status(int reset);
  * `timeout_ns` nanoseconds, on a shared-memory barrier that nothing completes, then gives
  * up, records RA_ERR_DEVICE_TIMEOUT in the device status and returns. */
 int ra_test_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* Test hook for the softmax's FMA-pipe exponential: y[i] = 2^x[i] for n device floats
+ * x[i] <= 127, computed the way the forward kernel computes part of its exponentials
+ * (range split and a degree-3 polynomial; relative error below 8e-5; inputs below -125
+ * give 2^-125). */
+int ra_test_exp2_poly(const float* x, float* y, int n, void* stream);
 
 /* Profiling hook: while set (non-NULL), ra_ring_attn_fwd and ra_ring_attn_bwd record
  * `start_event` immediately before and `stop_event` immediately after their main kernel

@@ -90,7 +90,20 @@ def test_cuda_core_cross_check_path(w, monkeypatch):
         assert_grad(w, name, res[name], ref)
 
 
-@pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[7], F32[1]], ids=lambda w: w.name)
+# f32 head dims whose rows do not fill a warp evenly (48 and 96: 12 and 24 four-element
+# pieces; 18: not a multiple of 4, one element per lane) exercise the merge's row split.
+MERGE_F32 = [
+    wl("f32_merge_dh48", dtype="f32", layout="zigzag", D=4, hq=4, hkv=2, dh=48,
+       seqlens=(40, 96, 8), seed=24),
+    wl("f32_merge_dh96", dtype="f32", layout="basic", D=2, hq=2, hkv=1, dh=96, batch=2,
+       seqlen=72, seed=25),
+    wl("f32_merge_dh18", dtype="f32", layout="stripe", D=3, hq=3, hkv=3, dh=18, batch=1,
+       seqlen=66, seed=26),
+]
+
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[2], SMALL[7], F32[1]] + MERGE_F32,
+                         ids=lambda w: w.name)
 @pytest.mark.parametrize("block_dtype", [torch.float32, torch.bfloat16])
 def test_unfused_steps_and_merge(w, block_dtype):
     """Per-step block_attn_fwd equals the oracle's block of every (rank, step); merging the
@@ -207,3 +220,115 @@ def test_repeated_calls_are_stable():
     res2, _ = run(w, inputs=inputs, backward=False)
     np.testing.assert_array_equal(res1["out"], res2["out"])
     np.testing.assert_array_equal(res1["lse"], res2["lse"])
+
+
+# ---------------------------------------------------------------------------------------
+# unfused backward: one ring step at a time
+# ---------------------------------------------------------------------------------------
+
+def _shard_major_inputs(w):
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    qd, kd, vd, dod = (upload(x, w) for x in (q, k, v, do))
+    prob = problem(w, qd, kd)
+    qs, ks, vs, dos = (ra.shard_tokens(x, prob) for x in (qd, kd, vd, dod))
+    rows = LY.shard_major_rows(w.layout, w.D, w.lengths, w.varlen)
+    host = tuple(LY.shard(packed(x).astype(np.float64), rows, 0) for x in (q, k, v, do))
+    return prob, (qs, ks, vs, dos), host, rows
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], SMALL[7], SMALL[8], F32[1]], ids=lambda w: w.name)
+def test_block_backward_per_step_matches_oracle(w):
+    """ra_block_attn_bwd of every step (all ranks), each added into zeroed float32
+    accumulators, equals the oracle's per-step terms of the ring backward; the sum over the
+    steps equals the fused backward."""
+    prob, (qs, ks, vs, dos), (q_h, k_h, v_h, do_h), rows = _shard_major_inputs(w)
+    out_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, prob)
+    o_h = packed(out_s.float().cpu().numpy()).astype(np.float64)
+    l_h = lse_s.cpu().numpy().astype(np.float64)
+    l_h = l_h if w.varlen else l_h.transpose(1, 0, 2).reshape(w.hq, -1)
+    tot = [torch.zeros(t.shape, device="cuda") for t in (qs, ks, vs)]
+    for s in range(w.D):
+        acc = [torch.zeros(t.shape, device="cuda") for t in (qs, ks, vs)]
+        ra.block_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob, -1, s, *acc)
+        ref = R.ring_bwd(q_h, k_h, v_h, o_h, l_h, do_h, w.lengths, w.D, w.layout, w.causal,
+                         w.varlen, steps=[s])
+        for name, a, r_ in zip(("dq", "dk", "dv"), acc, ref):
+            assert_grad(w, f"{name} step {s}", packed(a.cpu().numpy()), r_)
+        for t, a in zip(tot, acc):
+            t += a
+    fused = ra.ring_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob)
+    for name, t, f in zip(("dq", "dk", "dv"), tot, fused):
+        assert_grad(w, f"{name} sum of steps", packed(t.cpu().numpy()), packed(f.float().cpu().numpy()))
+    assert ra.check_device_status() == 0, ra.last_error()
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[7]], ids=lambda w: w.name)
+def test_block_backward_single_rank(w):
+    """One (rank, step) call touches only that rank's dq rows and shard (rank - step) mod
+    D's dk / dv rows, and matches the oracle's term of that pair."""
+    prob, (qs, ks, vs, dos), (q_h, k_h, v_h, do_h), rows = _shard_major_inputs(w)
+    out_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, prob)
+    o_h = packed(out_s.float().cpu().numpy()).astype(np.float64)
+    l_h = lse_s.cpu().numpy().astype(np.float64)
+    l_h = l_h if w.varlen else l_h.transpose(1, 0, 2).reshape(w.hq, -1)
+    sentinel = 0.5
+    for r, s in ((1, 0), (2, 3), (3, 1)):
+        acc = [torch.full(t.shape, sentinel, device="cuda") for t in (qs, ks, vs)]
+        ra.block_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob, r, s, *acc)
+        ref = R.ring_bwd(q_h, k_h, v_h, o_h, l_h, do_h, w.lengths, w.D, w.layout, w.causal,
+                         w.varlen, steps=[s], ranks=[r])
+        j = (r - s) % w.D
+        mine_q = np.concatenate([R.piece_rows(w.lengths, w.D, w.varlen, i, r) for i in range(len(w.lengths))])
+        mine_k = np.concatenate([R.piece_rows(w.lengths, w.D, w.varlen, i, j) for i in range(len(w.lengths))])
+        for name, a, r_, mine in zip(("dq", "dk", "dv"), acc, ref, (mine_q, mine_k, mine_k)):
+            a = packed(a.cpu().numpy()).astype(np.float64)
+            others = np.setdiff1d(np.arange(a.shape[0]), mine)
+            assert np.all(a[others] == sentinel), name
+            assert_grad(w, name, a[mine] - sentinel, r_[mine])
+
+
+# ---------------------------------------------------------------------------------------
+# deterministic backward
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w", [SMALL[0], SMALL[1], SMALL[3], SMALL[7], SMALL[10]], ids=lambda w: w.name)
+def test_deterministic_backward_is_bitwise_repeatable(w):
+    """deterministic = 1 (tensor-core K/V pass + query-tile dq pass, no atomics): parity
+    with the oracle, and two runs give bit-identical dq, dk, dv."""
+    q, k, v = W.make_qkv(w)
+    do = W.make_dout(w)
+    qd, kd, vd, dod = (upload(x, w) for x in (q, k, v, do))
+    prob = ra.problem_for(qd, kd, D=w.D, layout=w.layout, causal=w.causal,
+                          cu_seqlens=w.cu_seqlens if w.varlen else None, deterministic=True)
+    assert ra.workspace_bytes(prob) < ra.workspace_bytes(problem(w, qd, kd))  # no dq sums
+    qs, ks, vs, dos = (ra.shard_tokens(x, prob) for x in (qd, kd, vd, dod))
+    out_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, prob)
+    g1 = [t.clone() for t in ra.ring_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob)]
+    g2 = ra.ring_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = A.attention_bwd(packed(q), packed(k), packed(v), packed(do), w.cu_seqlens, w.causal)
+    for name, g, r_ in zip(("dq", "dk", "dv"), g1, ref):
+        assert_grad(w, name, ra.unshard_tokens(g, prob).float().cpu().numpy(), r_)
+    assert ra.check_device_status() == 0, ra.last_error()
+
+
+def test_fma_pipe_exp2_error_bound():
+    """The forward's FMA-pipe 2^x (range split + fitted cubic) stays within its stated
+    relative error bound against float64 2^x over the softmax's input range, and clamps
+    below -125."""
+    x = np.concatenate([np.linspace(-125.0, 8.0, 200001), np.linspace(-0.5, 0.5, 10001),
+                        np.arange(-20, 9, dtype=np.float64)]).astype(np.float32)
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    ra._abi.check(ra._abi.lib().ra_test_exp2_poly(ra.ops._p(xd), ra.ops._p(yd), x.size,
+                                                  ra.ops._stream()))
+    y = yd.cpu().numpy().astype(np.float64)
+    ref = np.exp2(x.astype(np.float64))
+    rel = np.abs(y / ref - 1.0)
+    assert rel.max() < 8e-5, rel.max()
+    low = torch.tensor([-126.0, -1000.0, float("-inf")], device="cuda")
+    out = torch.empty_like(low)
+    ra._abi.check(ra._abi.lib().ra_test_exp2_poly(ra.ops._p(low), ra.ops._p(out), 3, ra.ops._stream()))
+    np.testing.assert_allclose(out.cpu().numpy(), np.exp2(-125.0) * np.ones(3), rtol=1e-4)
