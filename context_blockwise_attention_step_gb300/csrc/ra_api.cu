@@ -184,6 +184,15 @@ bool force_simt() {
 
 bool use_tc(const ra_problem* p) { return p->dtype == RA_BF16 && !force_simt(); }
 
+// The tensor-core backward runs as two atomic-free passes (K/V tiles for dk / dv, query
+// tiles for dq), which is both faster and run-to-run deterministic. RA_BWD=fused selects
+// the single K/V-tile pass that adds dq with float reductions instead (for comparison;
+// never used for problems that ask for determinism).
+bool fused_bwd(const ra_problem* p) {
+  const char* e = getenv("RA_BWD");
+  return use_tc(p) && !p->deterministic && e != nullptr && strcmp(e, "fused") == 0;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t delta_bytes(const ra_problem* p) {
@@ -193,7 +202,7 @@ size_t delta_bytes(const ra_problem* p) {
 }
 
 size_t dq_acc_bytes(const ra_problem* p) {
-  if (!use_tc(p) || p->deterministic) return 0;
+  if (!fused_bwd(p)) return 0;
   int64_t rows = 0;
   for (int64_t x : lengths_of(p)) rows += x;
   return align256(size_t(rows) * p->hq * p->head_dim * sizeof(float));
@@ -291,7 +300,7 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
   PlanHolder E(make_plan(p, 2, 0, p->D, -1, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  if (use_tc(p) && p->deterministic) {
+  if (use_tc(p) && !fused_bwd(p)) {
     // dk, dv from the K/V-tile kernel without its dq part; dq query-tile-major
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
     e = profiled(st, [&] {

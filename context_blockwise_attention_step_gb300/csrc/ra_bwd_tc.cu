@@ -151,6 +151,30 @@ __device__ __forceinline__ void add_row32_f32(float* dst, const uint32_t (&r)[32
   }
 }
 
+// 8 x 8 transpose of 16-byte pieces inside each group of 8 lanes: on entry lane t of a
+// group holds pieces 0..7 (r[4j..4j+3]) of its own row; on exit it holds piece t of the
+// group's rows 0..7 (r[4j..4j+3] = piece t of row j). Three butterfly stages (lane
+// distance 4, 2, 1): at distance s the lanes with bit s clear keep the pieces whose index
+// has bit s clear and take the partner's, and the other lanes the reverse.
+__device__ __forceinline__ void transpose8_f4(uint32_t (&r)[32], int t) {
+#pragma unroll
+  for (int s = 4; s >= 1; s >>= 1) {
+    const bool hi = (t & s) != 0;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; ++j0) {
+      if (j0 & s) continue;
+      const int j1 = j0 | s;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t send = hi ? r[4 * j0 + e] : r[4 * j1 + e];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, send, s);
+        if (hi) r[4 * j0 + e] = got;
+        else r[4 * j1 + e] = got;
+      }
+    }
+  }
+}
+
 // One 32-column chunk of dS^T = P^T * (dP^T - delta) for the query columns
 // [c0 + 32*CH, c0 + 32*CH + 32) of this thread's K/V row: reads dP^T from Y, writes the
 // bf16 result to Y columns [32 + c0/2 + 16*CH, +16) (the A operand of the dK MMA) and,
@@ -337,6 +361,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           issue_S(sQ0 + st * C::kStageBytes);
         }
         int i = 0;
+        if constexpr (!kWithDQ) {
+          // Without dQ the order per tile is [dS(i-1)] dK(i-1), dP(i), [P(i)] dV(i), S(i+1):
+          // dP(i) needs no P, so it runs while P(i) is computed, and S(i+1) runs while
+          // dS(i) is computed.
+          ok = for_each_qtile(P, it, wk, [&](int, int, int) -> bool {
+            const int qi = qc + i;
+            const int st = qi & 1;
+            const uint32_t sQ = sQ0 + st * C::kStageBytes, sDO = sQ + C::kTileBytes;
+            if (i > 0) {
+              if (!mbar_wait(&sh.ds_full, ds_phase, abort_flag, tmo, status)) return false;
+              ds_phase ^= 1;
+              tc_fence_after();
+              const uint32_t sQp = sQ0 + ((qi - 1) & 1) * C::kStageBytes;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQp + k * 2048, kSubBytes, 1024),
+                       idKV, (i > 1 || k > 0) ? 1u : 0u);
+              tc_commit(&sh.q_empty[(qi - 1) & 1]);
+            }
+#pragma unroll
+            for (int k = 0; k < C::kKSteps; ++k) {
+              const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+              mma_ss(tY, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), idSS, k > 0);
+            }
+            tc_commit(&sh.dp_full);
+            if (!mbar_wait(&sh.p_full, p_phase, abort_flag, tmo, status)) return false;
+            p_phase ^= 1;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::kColDV, tX + 32 + 8 * k, sdesc_sw128(sDO + k * 2048, kSubBytes, 1024),
+                     idKV, (i > 0 || k > 0) ? 1u : 0u);
+            if (i + 1 < wk.N) {
+              const int st1 = (qi + 1) & 1;
+              if (!mbar_wait(&sh.q_full[st1], ((qi + 1) >> 1) & 1, abort_flag, tmo, status)) return false;
+              tc_fence_after();
+              issue_S(sQ0 + st1 * C::kStageBytes);
+            }
+            ++i;
+            return true;
+          });
+          if (ok) {  // the last tile's dK
+            const int ql = qc + wk.N - 1;
+            ok = mbar_wait(&sh.ds_full, ds_phase, abort_flag, tmo, status);
+            ds_phase ^= 1;
+            tc_fence_after();
+            const uint32_t sQl = sQ0 + (ql & 1) * C::kStageBytes;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQl + k * 2048, kSubBytes, 1024),
+                     idKV, (wk.N > 1 || k > 0) ? 1u : 0u);
+            tc_commit(&sh.q_empty[ql & 1]);
+          }
+          if (!ok) break;
+          qc += wk.N;
+          tc_commit(&sh.acc_done);
+          tc_commit(&sh.kv_empty);
+          continue;
+        }
         ok = for_each_qtile(P, it, wk, [&](int, int, int) -> bool {
           const int qi = qc + i;
           const int st = qi & 1;
@@ -546,10 +629,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!mbar_wait(&sh.dq_full, dqf_phase, abort_flag, tmo, status)) return false;
           dqf_phase ^= 1;
           tc_fence_after();
-          const int a = q0 + row;
-          const bool valid = a < wk.L;
-          float* dst =
-              dq_acc + (static_cast<size_t>(sd.row_off + r * P.shard_stride + a) * P.hq + h) * DH;
+          // Lane 8g + t ends up with 16-byte piece t of rows 8g .. 8g+7 of its warp's 32
+          // rows, so each reduction instruction covers four rows x 128 contiguous bytes.
+          const int t8 = lane & 7;
+          const int row0 = q0 + quarter * 32 + (lane & ~7);  // first row of this lane's group
+          const size_t base = static_cast<size_t>(sd.row_off + r * P.shard_stride);
 #pragma unroll
           for (int c = 0; c < DH / 32; ++c) {
             uint32_t rr[32];
@@ -558,12 +642,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               tc_fence_before();
               mbar_arrive(&sh.dq_free);
             }
-            if (valid) {
+            transpose8_f4(rr, t8);
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                red_add_v4(dst + c * 32 + 4 * q, __uint_as_float(rr[4 * q]) * mul,
-                           __uint_as_float(rr[4 * q + 1]) * mul, __uint_as_float(rr[4 * q + 2]) * mul,
-                           __uint_as_float(rr[4 * q + 3]) * mul);
+            for (int j = 0; j < 8; ++j) {
+              const int a = row0 + j;
+              if (a < wk.L) {
+                float* dst = dq_acc + ((base + a) * P.hq + h) * DH + c * 32 + 4 * t8;
+                red_add_v4(dst, __uint_as_float(rr[4 * j]) * mul, __uint_as_float(rr[4 * j + 1]) * mul,
+                           __uint_as_float(rr[4 * j + 2]) * mul, __uint_as_float(rr[4 * j + 3]) * mul);
+              }
             }
           }
           return true;

@@ -40,6 +40,11 @@ static __device__ unsigned int g_status_fwd;
 namespace {
 
 constexpr int kFwdThreads = 384;
+// Of every 8 pairs of softmax exponentials, this many are evaluated on the FMA pipe
+// (exp2_poly2) and the rest on the MUFU unit.
+#ifndef RA_FWD_POLY_PAIRS
+#define RA_FWD_POLY_PAIRS 3
+#endif
 constexpr int kSubBytes = 128 * 128;  // 128 rows x 64 bf16: one 128B-swizzled sub-tile
 
 template <int DH>
@@ -358,8 +363,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (grow) m = m_new;
           const float mref = (m == -INFINITY) ? 0.f : m;
           // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs over the consumed S columns.
-          // Three pairs in eight take 2^x from the FMA pipe (exp2_poly2), the rest from the
-          // MUFU unit, so that neither unit limits the tile rate.
+          // RA_FWD_POLY_PAIRS pairs in eight take 2^x from the FMA pipe (exp2_poly2), the
+          // rest from the MUFU unit, so that neither unit limits the tile rate.
           const uint64_t nm2 = f2(-mref, -mref);
           uint64_t l2 = f2(0.f, 0.f);
 #pragma unroll
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int i = 0; i < 16; ++i) {
               const uint64_t x = fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, nm2);
               uint64_t p2;
-              if ((i & 7) < 3) {
+              if ((i & 7) < RA_FWD_POLY_PAIRS) {
                 p2 = exp2_poly2(x);
               } else {
                 const float2 e = f2_split(x);

@@ -1,7 +1,7 @@
 // ra_noalloc.cu — a backward entry point for callers that cannot allocate device memory.
 //
-// ra_ring_attn_bwd needs scratch memory (float32 dq partial sums and the per-row
-// dot(dout, out)) that its caller passes in. Some callers cannot provide it: a plain-C
+// ra_ring_attn_bwd needs scratch memory (the per-row dot(dout, out), and float32 dq
+// partial sums for its single-pass variant) that its caller passes in. Some callers cannot provide it: a plain-C
 // plugin that its host framework hands only the input and output buffers, or a caller
 // whose allocator forbids cudaMalloc (and its device-wide synchronisation) inside a
 // training step. For them this file keeps the scratch in one file-scope device array of

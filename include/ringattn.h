@@ -89,8 +89,10 @@ typedef struct ra_problem {
   int32_t head_dim;           /* Dh                                                         */
   float scale;                /* softmax scale; <= 0 selects 1/sqrt(head_dim) (the pages'
                                  default for scaling=None)                                  */
-  int32_t deterministic;      /* 1: backward without floating-point atomics (run-to-run
-                                 bit-identical dq). 0: dq accumulated with atomics          */
+  int32_t deterministic;      /* 1: the backward must be run-to-run bit-identical (no
+                                 floating-point atomics). 0: no such promise is asked for;
+                                 the bf16 backward is atomic-free and deterministic anyway,
+                                 the f32 one always is                                      */
 } ra_problem;
 
 /* Fused ring forward: every rank r, every step s = 0..D-1 against K/V shard (r-s) mod D,
@@ -130,9 +132,12 @@ size_t ra_workspace_bytes(const ra_problem* p, int which);
  * forward (P recomputed from lse, never stored); dq accumulates per query rank, dk and dv
  * accumulate into the K/V shard that owns the block, summed over the query heads of a
  * group. Inputs: q, k, v, out, lse as from the forward, dout like out. Outputs dq (like q),
- * dk, dv (like k) in the problem dtype; every element is written. The workspace (device,
- * >= ra_workspace_bytes(p, 1), 256-byte aligned) holds float32 dq partial sums and the
- * per-row dot(dout, out); it is overwritten. */
+ * dk, dv (like k) in the problem dtype; every element is written. The bf16 path runs two
+ * passes without atomics (K/V tiles: dk, dv; query tiles: dq), so results are run-to-run
+ * bit-identical. The workspace (device, >= ra_workspace_bytes(p, 1), 256-byte aligned)
+ * holds the per-row dot(dout, out) (and, only when the environment variable RA_BWD=fused
+ * selects the single-pass variant with float reductions, float32 dq sums); it is
+ * overwritten. */
 int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const void* v,
                      const void* out, const float* lse, const void* dout, void* dq,
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
@@ -159,7 +164,8 @@ int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, co
  * handed only its input and output buffers, or a caller that must keep cudaMalloc and its
  * device-wide synchronisation out of a training step). The pages have no counterpart: on
  * the pages every rank allocates its own buffers. Instead of a caller workspace, the
- * scratch (f32 dq partial sums and per-row dot(dout, out)) lives in one static device
+ * scratch (the per-row dot(dout, out), plus float32 dq sums when RA_BWD=fused selects the
+ * single-pass variant) lives in one static device
  * array of RA_NOALLOC_SCRATCH_BYTES that every GPU loading the library keeps until exit.
  * Arguments as for ra_ring_attn_bwd minus the workspace. Problems whose
  * ra_workspace_bytes(p, 1) exceeds the array are rejected with RA_ERR_WORKSPACE and nothing

@@ -76,12 +76,16 @@ def test_null_pointers_rejected_without_launch(built_library):
     assert built_library.ra_block_attn_fwd(p.ptr, 9, 0, *([None] * 4), 0, None, None) == _abi.RA_ERR_INVALID_ARG
 
 
-def test_workspace_size_and_check():
+def test_workspace_size_and_check(monkeypatch):
     p = _prob()
     need = ra.workspace_bytes(p, 1)
     rows, hq, dh = 2 * 64, 8, 128
-    assert need >= rows * hq * 4 + rows * hq * dh * 4
+    assert need >= rows * hq * 4  # per-row dot(dout, out)
+    assert ra.workspace_bytes(p, 2) >= rows * hq * 4
     assert ra.workspace_bytes(p, 0) == 0
+    monkeypatch.setenv("RA_BWD", "fused")  # the single-pass variant also needs float32 dq sums
+    assert ra.workspace_bytes(p, 1) >= rows * hq * 4 + rows * hq * dh * 4
+    monkeypatch.delenv("RA_BWD")
     lib = _abi.lib()
     fake = 256  # never dereferenced: the size check fails first
     st = lib.ra_ring_attn_bwd(p.ptr, *([fake] * 9), fake, need - 1, None)

@@ -8,7 +8,10 @@ are checked on outputs the oracle computes one by one:
   of the layout plus random rows): each is exact from its own row of scores;
 * dk and dv on the K/V rows of the last 128 positions of every sequence: under the causal
   rule only the last 128 queries see them, so those queries' gradients give them exactly;
-* at any size: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per K/V head and sequence.
+* at any size: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per K/V head and sequence;
+* for the 32K (one head), varlen 64K and 128K (one group of four query heads) workloads,
+  dq, dk and dv of one whole K/V-head group, every row, against the oracle's backward of
+  that group (run over row chunks in spawned processes).
 """
 import numpy as np
 import pytest
@@ -20,6 +23,7 @@ from oracle import attention as A
 from oracle import layouts as LY
 
 from _gpu_path import assert_grad, assert_lse, assert_out, packed, run
+from _oracle_pool import group_backward
 
 pytestmark = pytest.mark.gpu
 
@@ -78,6 +82,8 @@ def tail_rows(w: W.Workload, width=128):
     return np.array(rows, dtype=np.int64)
 
 
+FULL_GROUP = {W.LONG32K.name, W.VARLEN.name, W.LONG128K.name}
+
 LARGE = [W.LONG32K, W.LONG32K.with_layout("stripe"), W.VARLEN, W.VARLEN.with_layout("basic"),
          W.VARLEN.with_layout("stripe"), W.LONG128K]
 
@@ -108,3 +114,10 @@ def test_large_workload_sampled(w):
         want = dop[s0:s1].astype(np.float64).reshape(s1 - s0, w.hkv, g, w.head_dim).sum(axis=(0, 2))
         got = gdv[s0:s1].sum(axis=0)
         assert np.linalg.norm(got - want) <= 2e-2 * np.linalg.norm(want) + 1e-3
+    # every row of one whole K/V-head group
+    if w.name in FULL_GROUP:
+        hk = w.hkv - 1
+        dq_g, dk_g, dv_g = group_backward(qp, kp, vp, dop, cu, True, hk, g)
+        assert_grad(w, "dq (group)", packed(res["dq"])[:, hk * g:(hk + 1) * g], dq_g)
+        assert_grad(w, "dk (group)", packed(res["dk"])[:, hk:hk + 1], dk_g)
+        assert_grad(w, "dv (group)", packed(res["dv"])[:, hk:hk + 1], dv_g)

@@ -28,8 +28,8 @@ def _case():
 
 def test_oversized_problem_is_rejected_without_launch():
     ra.build()
-    big = ra.make_problem(dtype=torch.bfloat16, layout="basic", causal=True, D=1, hq=32, hkv=8,
-                          head_dim=128, batch=1, seqlen=8192)
+    big = ra.make_problem(dtype=torch.bfloat16, layout="basic", causal=True, D=1, hq=64, hkv=8,
+                          head_dim=128, batch=1, seqlen=524288)
     assert ra.workspace_bytes(big) > _abi.RA_NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
     st = _abi.lib().ra_ring_attn_bwd_noalloc(big.ptr, *([fake] * 9), None)
