@@ -238,6 +238,7 @@ def run_ours(args, rank, world, local_rank):
     sp = [ev() for _ in range(args.steps)]
     kf = [(ev(), ev()) for _ in range(args.steps)]
     kb = [(ev(), ev()) for _ in range(args.steps)]
+    km = [ev() for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -249,8 +250,10 @@ def run_ours(args, rank, world, local_rank):
             ra.profile_events(*kf[i])
             ra.ring_attn_fwd(qs, ks, vs, prob, out=out, lse=lse)
             ra.profile_events(*kb[i])
+            ra.profile_split_event(km[i])
             ra.ring_attn_bwd(dos, qs, ks, vs, out, lse, prob, dq=dq, dk=dk, dv=dv, workspace=ws)
             ra.profile_events(None, None)
+            ra.profile_split_event(None)
             sp[i].record(stream)
         torch.cuda.synchronize(dev)
     if dist is not None:
@@ -258,6 +261,7 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(b) for a, b in zip(st, sp)]
     fwd_ms = [a.elapsed_time(b) for a, b in kf]
     bwd_ms = [a.elapsed_time(b) for a, b in kb]
+    kv_ms = [a.elapsed_time(m) for (a, _), m in zip(kb, km)]
     if ra.check_device_status() != 0:
         raise RuntimeError(f"device status after the timed region: {ra.last_error()}")
 
@@ -295,10 +299,12 @@ def run_ours(args, rank, world, local_rank):
     secondary = measure_secondary(ra, w, nat, prob, (qs, ks, vs, dos), ev, stream) if args.secondary else None
 
     per = torch.tensor([sum(step_ms) / args.steps, e2e_ms, statistics.mean(fwd_ms),
-                        statistics.mean(bwd_ms)], device=dev, dtype=torch.float64)
+                        statistics.mean(bwd_ms), statistics.mean(kv_ms)], device=dev,
+                       dtype=torch.float64)
     if dist is not None:
         dist.all_reduce(per, op=dist.ReduceOp.MAX)
-    ms_step, e2e_ms, fwd_mean, bwd_mean = per.tolist()
+    ms_step, e2e_ms, fwd_mean, bwd_mean, kv_mean = per.tolist()
+    dq_mean = bwd_mean - kv_mean
 
     ff, fb = fwd_bwd_flops(w)
     value = world * (ff + fb) / (ms_step * 1e-3) / 1e12
@@ -311,18 +317,30 @@ def run_ours(args, rank, world, local_rank):
     mtr = TRAFFIC.get(("merge_kernel", w.name))
     merge["traffic"] = (mtr["bytes"] if mtr and mtr["source_sha"] == kernel_source_hash("ra_misc.cu")
                         else None)
+    # Algorithmic FLOP per kernel: the forward's 2 GEMMs; of the backward's 5 (S recompute,
+    # dP, dV, dK, dQ) the K/V-tile pass does 4 and the dq pass adds dQ (its S and dP
+    # recomputation is executed work the method does not count).
     kern = {
-        "ring_fwd_tc": {"ms": fwd_mean, "tflops": ff / (fwd_mean * 1e-3) / 1e12,
-                        "algorithmic_tflop_per_launch": ff / 1e12},
-        "ring_bwd_tc": {"ms": bwd_mean, "tflops": fb / (bwd_mean * 1e-3) / 1e12,
-                        "algorithmic_tflop_per_launch": fb / 1e12},
+        "ring_fwd_tc": {"ms": fwd_mean, "algorithmic_tflop_per_launch": ff / 1e12,
+                        "executed_tflop_per_launch": ff / 1e12},
+        "ring_bwd_tc (K/V-tile pass)": {"ms": kv_mean, "algorithmic_tflop_per_launch": 2.0 * ff / 1e12,
+                                        "executed_tflop_per_launch": 2.0 * ff / 1e12},
+        "ring_bwd_dq_tc (dq pass)": {"ms": dq_mean, "algorithmic_tflop_per_launch": 0.5 * ff / 1e12,
+                                     "executed_tflop_per_launch": 1.5 * ff / 1e12},
     }
     for kv in kern.values():
+        kv["tflops"] = kv["algorithmic_tflop_per_launch"] / (kv["ms"] * 1e-3)
+        kv["executed_tflops"] = kv["executed_tflop_per_launch"] / (kv["ms"] * 1e-3)
         kv["frac_of_sustained_peak"] = kv["tflops"] / peak_sus
         kv["frac_of_burst_peak"] = kv["tflops"] / peak_burst
+        kv["executed_frac_of_sustained_peak"] = kv["executed_tflops"] / peak_sus
         kv["share_of_step"] = kv["ms"] / ms_step
+    backward = {"ms": bwd_mean, "tflops": fb / (bwd_mean * 1e-3) / 1e12,
+                "algorithmic_tflop": fb / 1e12}
+    backward["frac_of_sustained_peak"] = backward["tflops"] / peak_sus
     dom = max(kern, key=lambda n: kern[n]["ms"])
-    src = {"ring_fwd_tc": "ra_fwd_tc.cu", "ring_bwd_tc": "ra_bwd_tc.cu"}[dom]
+    src = {"ring_fwd_tc": "ra_fwd_tc.cu", "ring_bwd_tc (K/V-tile pass)": "ra_bwd_tc.cu",
+           "ring_bwd_dq_tc (dq pass)": "ra_bwd_dq_tc.cu"}[dom]
     tr = TRAFFIC.get((dom, w.name))
     traffic = tr["bytes"] if tr and tr["source_sha"] == kernel_source_hash(src) else None
     result = None
@@ -354,14 +372,18 @@ def run_ours(args, rank, world, local_rank):
                          "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peak_sus,
                          "frac_burst": kern[dom]["tflops"] / peak_burst,
                          "traffic": traffic,
-                         "algorithmic_unit": "2.5 x 4 x head_dim FLOP per causal (query, key) pair"},
+                         "algorithmic_unit": "2 x head_dim FLOP per causal (query, key) pair for "
+                                             "each of the path's seven GEMMs (fwd QK^T, PV; bwd S, "
+                                             "dP, dV, dK, dQ) the kernel performs, over S^2/2 pairs "
+                                             "per sequence and query head"},
             "kernels": kern,
+            "backward_both_passes": backward,
             "merge_kernel": merge,
             "secondary": secondary,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 4 * args.steps,  # forward; backward preprocess, K/V pass, dq pass
             "clocks": clocks.summary(),
             "step_ms": step_ms,
         }

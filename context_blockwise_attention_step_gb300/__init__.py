@@ -11,6 +11,6 @@ from .ops import (  # noqa: F401
     block_attn_fwd, block_attn_bwd,
     update_out_and_lse, workspace_bytes, shard_tokens, unshard_tokens, shard_lse, unshard_lse,
     validate, layout_positions, step_counts, work_items, check_device_status,
-    test_wait_timeout, profile_events, last_error, version,
+    test_wait_timeout, profile_events, profile_split_event, last_error, version,
 )
 from .autograd import RingSelfAttention, ring_attention, shard, unshard  # noqa: F401,E402

@@ -27,7 +27,8 @@ EXPORTS = (
     "ra_ring_attn_fwd", "ra_block_attn_fwd", "ra_update_out_and_lse", "ra_workspace_bytes",
     "ra_ring_attn_bwd", "ra_block_attn_bwd", "ra_ring_attn_bwd_noalloc", "ra_shard_tokens", "ra_shard_lse", "ra_validate",
     "ra_layout_positions", "ra_step_counts", "ra_work_items", "ra_check_device_status",
-    "ra_test_wait_timeout", "ra_test_exp2_poly", "ra_profile_events", "ra_last_error",
+    "ra_test_wait_timeout", "ra_test_exp2_poly", "ra_profile_events", "ra_profile_split_event",
+    "ra_last_error",
     "ra_version",
 )
 
@@ -90,6 +91,7 @@ def lib() -> ctypes.CDLL:
         "ra_test_wait_timeout": (i32, [ctypes.c_uint64, vp]),
         "ra_test_exp2_poly": (i32, [vp, vp, i32, vp]),
         "ra_profile_events": (i32, [vp, vp]),
+        "ra_profile_split_event": (i32, [vp]),
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_version": (i32, []),
     }

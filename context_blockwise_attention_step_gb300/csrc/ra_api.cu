@@ -25,7 +25,7 @@ using ra::SeqDesc;
 namespace {
 
 thread_local std::string g_last_error;
-thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr, g_prof_mid = nullptr;
 
 // Records the profiling events (if set) around the launch done by `launch`.
 template <typename F>
@@ -304,11 +304,13 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
     // dk, dv from the K/V-tile kernel without its dq part; dq query-tile-major
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
     e = profiled(st, [&] {
-      return ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvOnly, q, k, v, dout, lse, delta, nullptr, dk, dv, st);
+      cudaError_t r = ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvOnly, q, k, v, dout, lse, delta, nullptr,
+                                        dk, dv, st);
+      if (r != cudaSuccess) return r;
+      if (g_prof_mid) cudaEventRecord(g_prof_mid, st);
+      return ra::launch_bwd_dq_tc(*P.p, q, k, v, dout, lse, delta, dq, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    e = ra::launch_bwd_dq_tc(*P.p, q, k, v, dout, lse, delta, dq, st);
-    if (e != cudaSuccess) return cuda_fail(e, "backward dq launch");
   } else if (use_tc(p)) {
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes(p));
     e = cudaMemsetAsync(dq_acc, 0, dq_acc_bytes(p), st);
@@ -456,6 +458,11 @@ int ra_profile_events(void* start_event, void* stop_event) {
     return fail(RA_ERR_INVALID_ARG, "pass both events or neither");
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return ok();
+}
+
+int ra_profile_split_event(void* mid_event) {
+  g_prof_mid = static_cast<cudaEvent_t>(mid_event);
   return ok();
 }
 

@@ -34,6 +34,11 @@ static __device__ unsigned int g_status_dq;
 namespace {
 
 constexpr int kDqThreads = 384;
+// Of every 8 pairs of recomputed exponentials, this many are evaluated on the FMA pipe
+// (exp2_poly2) and the rest on the MUFU unit.
+#ifndef RA_DQ_POLY_PAIRS
+#define RA_DQ_POLY_PAIRS 0
+#endif
 constexpr int kSubBytes = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -328,18 +333,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!(ok = mbar_wait(&sh.s_full[buf], s_phase[buf], abort_flag, tmo, status))) break;
           s_phase[buf] ^= 1;
           tc_fence_after();
-          uint32_t pp[32];
+          uint32_t pp[32], sv2[2][32];
+          tmem_ld32_nowait(tS + c0, sv2[0]);  // both chunks in flight, one wait
+          tmem_ld32_nowait(tS + c0 + 32, sv2[1]);
+          tmem_wait_ld();
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             const int cs = c0 + 32 * ch;
-            uint32_t sv[32];
-            tmem_ld32(tS + cs, sv);
+            const uint32_t (&sv)[32] = sv2[ch];
             const bool full = __all_sync(0xffffffffu, cnt >= cs + 32);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float2 e = f2_split(
-                  fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, nl2));
-              float p0 = ex2(e.x), p1 = ex2(e.y);
+              const uint64_t x =
+                  fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, nl2);
+              float p0, p1;
+              if ((i & 7) < RA_DQ_POLY_PAIRS) {  // visible entries have x <= 0
+                const float2 e = f2_split(exp2_poly2(x));
+                p0 = e.x;
+                p1 = e.y;
+              } else {
+                const float2 e = f2_split(x);
+                p0 = ex2(e.x);
+                p1 = ex2(e.y);
+              }
               if (!full) {
                 if (cs + 2 * i >= cnt) p0 = 0.f;
                 if (cs + 2 * i + 1 >= cnt) p1 = 0.f;
@@ -350,11 +366,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (!(ok = mbar_wait(&sh.dp_full, dp_phase, abort_flag, tmo, status))) break;
           dp_phase ^= 1;
           tc_fence_after();
+          uint32_t dp2[2][32];
+          tmem_ld32_nowait(tmem + lane_off + C::kColDP + c0, dp2[0]);
+          tmem_ld32_nowait(tmem + lane_off + C::kColDP + c0 + 32, dp2[1]);
+          tmem_wait_ld();
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
             const int cs = c0 + 32 * ch;
-            uint32_t dp[32], o[16];
-            tmem_ld32(tmem + lane_off + C::kColDP + cs, dp);
+            const uint32_t (&dp)[32] = dp2[ch];
+            uint32_t o[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               uint64_t x = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), dl2);

@@ -30,10 +30,10 @@
 // backward); kAccum = true adds float32 dk / dv into the outputs instead of storing them
 // in the problem dtype (the per-step block backward of the unfused path).
 //
-// Warp roles (512 threads): warp 0 TMA producer (K, V once per item; Q and dO per query
-// tile, two stages), warp 1 TMEM allocator + MMA issuer, warp 2 lse / delta loader,
-// warps 4-7 and 8-11 the P / dS warpgroups (thread = K/V row; query columns 0-63 and
-// 64-127; at the end of an item they write dK and dV respectively), warps 12-15 the dQ
+// Warp roles (512 threads; 384 without dQ): warp 0 TMA producer (K, V once per item; Q and
+// dO per query tile, two stages), warp 1 TMEM allocator + MMA issuer, warp 2 lse / delta
+// loader, warps 4-7 and 8-11 the P / dS warpgroups (thread = K/V row; query columns 0-63
+// and 64-127; at the end of an item they write dK and dV respectively), warps 12-15 the dQ
 // warpgroup (thread = query row).
 #include <cuda_runtime.h>
 
@@ -47,7 +47,11 @@ static __device__ unsigned int g_status_bwd;
 
 namespace {
 
-constexpr int kBwdThreads = 512;
+// Of every 8 pairs of recomputed exponentials, this many are evaluated on the FMA pipe
+// (exp2_poly2) and the rest on the MUFU unit.
+#ifndef RA_BWD_POLY_PAIRS
+#define RA_BWD_POLY_PAIRS 0
+#endif
 constexpr int kSubBytes = 128 * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -175,16 +179,15 @@ __device__ __forceinline__ void transpose8_f4(uint32_t (&r)[32], int t) {
   }
 }
 
-// One 32-column chunk of dS^T = P^T * (dP^T - delta) for the query columns
-// [c0 + 32*CH, c0 + 32*CH + 32) of this thread's K/V row: reads dP^T from Y, writes the
-// bf16 result to Y columns [32 + c0/2 + 16*CH, +16) (the A operand of the dK MMA) and,
-// when dQ is computed, to the 128B-swizzled smem tile (the A operand of the dQ MMA).
+// dS^T = P^T * (dP^T - delta) for the 32 query columns [c0 + 32*CH, +32) of this thread's
+// K/V row, from their dP^T registers: the bf16 result goes to Y columns
+// [32 + c0/2 + 16*CH, +16) (the A operand of the dK MMA) and, when dQ is computed, to the
+// 128B-swizzled smem tile (the A operand of the dQ MMA).
 template <int CH, bool kWithDQ>
-__device__ __forceinline__ void ds_chunk(uint32_t tY, int c0, const float* dl,
-                                         const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
+__device__ __forceinline__ void ds_from(const uint32_t (&dp)[32], uint32_t tY, int c0, const float* dl,
+                                        const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
   const int cs = c0 + 32 * CH;
-  uint32_t dp[32], o[16];
-  tmem_ld32(tY + cs, dp);
+  uint32_t o[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 d2 = *reinterpret_cast<const float2*>(dl + cs + 2 * i);
@@ -207,25 +210,42 @@ __device__ __forceinline__ void ds_chunk(uint32_t tY, int c0, const float* dl,
   }
 }
 
-// One 32-column chunk of P^T = 2^(S^T * scale*log2e - lse*log2e) for query columns
-// [c0 + 32*CH, +32): columns before `lo` (queries that may not see this key) are zero;
-// columns past the sequence piece have -lse*log2e = -inf from the loader and give 0.
-// The bf16 result goes to X columns [32 + c0/2 + 16*CH, +16): inside the S^T columns this
-// warpgroup reads itself (the other warpgroup may still be reading its own), on columns
-// of a chunk this thread has already read (hence the per-warpgroup chunk order).
+// One chunk at a time (the output lands on dP^T columns this thread has already read, so the
+// chunk order differs between the two warpgroups).
+template <int CH, bool kWithDQ>
+__device__ __forceinline__ void ds_chunk(uint32_t tY, int c0, const float* dl,
+                                         const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
+  uint32_t dp[32];
+  tmem_ld32(tY + c0 + 32 * CH, dp);
+  ds_from<CH, kWithDQ>(dp, tY, c0, dl, pp, ds_row, row);
+}
+
+// P^T = 2^(S^T * scale*log2e - lse*log2e) for the query columns [c0 + 32*CH, +32), from
+// their S^T registers: columns before `lo` (queries that may not see this key) are zero;
+// columns past the sequence piece have -lse*log2e = -inf from the loader and give 0. The
+// bf16 result goes to X columns [32 + c0/2 + 16*CH, +16): inside the S^T columns this
+// warpgroup reads itself (the other warpgroup may still be reading its own).
 template <int CH>
-__device__ __forceinline__ void p_chunk(uint32_t tX, int c0, const float* nl, uint64_t sl2x2,
-                                        int lo, uint32_t (&pp)[32]) {
+__device__ __forceinline__ void p_from(const uint32_t (&sv)[32], uint32_t tX, int c0, const float* nl,
+                                       uint64_t sl2x2, int lo, uint32_t (&pp)[32]) {
   const int cs = c0 + 32 * CH;
-  uint32_t sv[32], pk[16];
-  tmem_ld32(tX + cs, sv);
+  uint32_t pk[16];
   const bool full = __all_sync(0xffffffffu, lo <= cs);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 n2 = *reinterpret_cast<const float2*>(nl + cs + 2 * i);
-    const float2 e = f2_split(
-        fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, f2(n2.x, n2.y)));
-    float p0 = ex2(e.x), p1 = ex2(e.y);
+    const uint64_t x = fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2,
+                            f2(n2.x, n2.y));
+    float p0, p1;
+    if ((i & 7) < RA_BWD_POLY_PAIRS) {  // visible entries have x <= 0; hidden ones are zeroed
+      const float2 e = f2_split(exp2_poly2(x));
+      p0 = e.x;
+      p1 = e.y;
+    } else {
+      const float2 e = f2_split(x);
+      p0 = ex2(e.x);
+      p1 = ex2(e.y);
+    }
     if (!full) {
       if (cs + 2 * i < lo) p0 = 0.f;
       if (cs + 2 * i + 1 < lo) p1 = 0.f;
@@ -236,8 +256,23 @@ __device__ __forceinline__ void p_chunk(uint32_t tX, int c0, const float* nl, ui
   tmem_st16(tX + 32 + c0 / 2 + 16 * CH, pk);
 }
 
+// One chunk at a time, on columns of a chunk this thread has already read (hence the
+// per-warpgroup chunk order).
+template <int CH>
+__device__ __forceinline__ void p_chunk(uint32_t tX, int c0, const float* nl, uint64_t sl2x2,
+                                        int lo, uint32_t (&pp)[32]) {
+  uint32_t sv[32];
+  tmem_ld32(tX + c0 + 32 * CH, sv);
+  p_from<CH>(sv, tX, c0, nl, sl2x2, lo, pp);
+}
+
+// Threads per block: the dQ warpgroup only exists when dq is computed; without it the
+// P / dS warpgroups get 170 registers a thread and load both of their chunks at once.
+template <bool kWithDQ>
+constexpr int bwd_threads() { return kWithDQ ? 512 : 384; }
+
 template <int DH, bool kWithDQ, bool kAccum>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     ring_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -561,7 +596,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         s_phase ^= 1;
         tc_fence_after();
         uint32_t pp[32];
-        if (wg == 0) {
+        if constexpr (!kWithDQ) {  // both chunks in registers before any write
+          uint32_t s0[32], s1[32];
+          tmem_ld32_nowait(tX + c0, s0);
+          tmem_ld32_nowait(tX + c0 + 32, s1);
+          tmem_wait_ld();
+          p_from<0>(s0, tX, c0, nl, sl2x2, lo, pp);
+          p_from<1>(s1, tX, c0, nl, sl2x2, lo, pp);
+        } else if (wg == 0) {
           p_chunk<1>(tX, c0, nl, sl2x2, lo, pp);
           p_chunk<0>(tX, c0, nl, sl2x2, lo, pp);
         } else {
@@ -576,7 +618,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&sh.dp_full, dp_phase, abort_flag, tmo, status)) return false;
         dp_phase ^= 1;
         tc_fence_after();
-        if (wg == 0) {
+        if constexpr (!kWithDQ) {
+          uint32_t d0[32], d1[32];
+          tmem_ld32_nowait(tY + c0, d0);
+          tmem_ld32_nowait(tY + c0 + 32, d1);
+          tmem_wait_ld();
+          ds_from<0, kWithDQ>(d0, tY, c0, dl, pp, ds_row, row);
+          ds_from<1, kWithDQ>(d1, tY, c0, dl, pp, ds_row, row);
+        } else if (wg == 0) {
           ds_chunk<1, kWithDQ>(tY, c0, dl, pp, ds_row, row);
           ds_chunk<0, kWithDQ>(tY, c0, dl, pp, ds_row, row);
         } else {
@@ -679,7 +728,8 @@ cudaError_t launch_one(const Plan& P, const CUtensorMap& mq, const CUtensorMap& 
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = P.n_items < n_sm ? P.n_items : n_sm;
-  kern<<<grid, kBwdThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta, dq_acc, dk, dv);
+  kern<<<grid, bwd_threads<kWithDQ>(), C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta, dq_acc,
+                                                            dk, dv);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@ constexpr int kFwdThreads = 384;
 // Of every 8 pairs of softmax exponentials, this many are evaluated on the FMA pipe
 // (exp2_poly2) and the rest on the MUFU unit.
 #ifndef RA_FWD_POLY_PAIRS
-#define RA_FWD_POLY_PAIRS 3
+#define RA_FWD_POLY_PAIRS 0
 #endif
 constexpr int kSubBytes = 128 * 128;  // 128 rows x 64 bf16: one 128B-swizzled sub-tile
 

@@ -34,8 +34,10 @@ long max_len(const Plan& P) {
 // ------------------------------------------------------------------ update_out_and_lse
 // lse' = log(e^lse + e^blse); out' = e^(lse-lse') out + e^(blse-lse') bout; -inf identity.
 // One warp per (row, head): lane 0 reads both lse values and broadcasts them, the lanes
-// walk the row in VEC-element pieces (VEC = 4 when head_dim % 4 == 0), and lane 0 writes
-// the merged lse only after the broadcast, so no lane can read an already-merged lse.
+// walk the row in VEC-element pieces (VEC = 4 when head_dim % 4 == 0; head_dim <= 128, so
+// one piece per lane), and lane 0 writes the merged lse only after the broadcast, so no
+// lane can read an already-merged lse. The row's out / block loads are issued before the
+// broadcast so that their latency overlaps the lse loads'.
 template <typename BT, int VEC>
 __global__ void __launch_bounds__(kThreads)
     merge_kernel(const __grid_constant__ Plan P, float* __restrict__ out, float* __restrict__ lse,
@@ -51,48 +53,64 @@ __global__ void __launch_bounds__(kThreads)
     const int a = static_cast<int>(x % L);
     const int r = P.rank_only >= 0 ? P.rank_only : static_cast<int>(x / L);
     const size_t li = lse_index(P, sd, h, r, a);
+    const size_t row = static_cast<size_t>(sd.row_off + r * P.shard_stride + a);
+    const size_t rb = (row * P.hq + h) * dh;
     float l1 = 0.f, l2 = 0.f;
     if (lane == 0) {
       l1 = lse[li];
       l2 = blse[li];
     }
-    l1 = __shfl_sync(0xffffffffu, l1, 0);
-    l2 = __shfl_sync(0xffffffffu, l2, 0);
-    const float mx = fmaxf(l1, l2);
-    float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
-    if (mx != -INFINITY) {
-      const float e1 = expf(l1 - mx), e2 = expf(l2 - mx);
-      const float s = e1 + e2;
-      lnew = mx + logf(s);
-      w1 = e1 / s;
-      w2 = e2 / s;
-    }
-    const size_t row = static_cast<size_t>(sd.row_off + r * P.shard_stride + a);
-    if (lane == 0) lse[li] = lnew;
-    if (mx == -INFINITY) continue;
-    for (int c = lane; c < nv; c += 32) {
-      const size_t e0 = (row * P.hq + h) * dh + static_cast<size_t>(c) * VEC;
-      if constexpr (VEC == 4) {
-        float4 o = *reinterpret_cast<float4*>(out + e0);
-        float b[4];
+    if constexpr (VEC == 4) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float b[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool mine = lane < nv;
+      if (mine) {
+        o = *reinterpret_cast<const float4*>(out + rb + 4 * lane);
         if constexpr (sizeof(BT) == 4) {
-          const float4 t = *reinterpret_cast<const float4*>(bout + e0);
+          const float4 t = *reinterpret_cast<const float4*>(bout + rb + 4 * lane);
           b[0] = t.x; b[1] = t.y; b[2] = t.z; b[3] = t.w;
         } else {
-          const uint2 t = *reinterpret_cast<const uint2*>(bout + e0);
+          const uint2 t = *reinterpret_cast<const uint2*>(bout + rb + 4 * lane);
           const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&t.x);
           const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&t.y);
           b[0] = __low2float(p0); b[1] = __high2float(p0);
           b[2] = __low2float(p1); b[3] = __high2float(p1);
         }
+      }
+      l1 = __shfl_sync(0xffffffffu, l1, 0);
+      l2 = __shfl_sync(0xffffffffu, l2, 0);
+      const float mx = fmaxf(l1, l2);
+      float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
+      if (mx != -INFINITY) {
+        const float e1 = expf(l1 - mx), e2 = expf(l2 - mx);
+        const float sum = e1 + e2;
+        lnew = mx + logf(sum);
+        w1 = e1 / sum;
+        w2 = e2 / sum;
+      }
+      if (lane == 0) lse[li] = lnew;
+      if (mine && mx != -INFINITY) {
         o.x = w1 * o.x + w2 * b[0];
         o.y = w1 * o.y + w2 * b[1];
         o.z = w1 * o.z + w2 * b[2];
         o.w = w1 * o.w + w2 * b[3];
-        *reinterpret_cast<float4*>(out + e0) = o;
-      } else {
-        out[e0] = w1 * out[e0] + w2 * ldf(bout + e0);
+        *reinterpret_cast<float4*>(out + rb + 4 * lane) = o;
       }
+    } else {
+      l1 = __shfl_sync(0xffffffffu, l1, 0);
+      l2 = __shfl_sync(0xffffffffu, l2, 0);
+      const float mx = fmaxf(l1, l2);
+      float w1 = 0.f, w2 = 0.f, lnew = -INFINITY;
+      if (mx != -INFINITY) {
+        const float e1 = expf(l1 - mx), e2 = expf(l2 - mx);
+        const float sum = e1 + e2;
+        lnew = mx + logf(sum);
+        w1 = e1 / sum;
+        w2 = e2 / sum;
+      }
+      if (lane == 0) lse[li] = lnew;
+      if (mx == -INFINITY) continue;
+      for (int c = lane; c < nv; c += 32) out[rb + c] = w1 * out[rb + c] + w2 * ldf(bout + rb + c);
     }
   }
 }

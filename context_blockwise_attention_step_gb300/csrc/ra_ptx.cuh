@@ -169,6 +169,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// The same 32-column load without the wait: several loads can be in flight before one
+// tmem_wait_ld() (the registers are valid only after it).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 // 32 lanes x 16 columns of 32-bit words, one lane per thread; waits for completion.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -266,8 +285,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // the softmax between the two units). Cody-Waite style split x = n + f with n = round(x)
 // taken from the low mantissa bits of x + 1.5*2^23, f in [-1/2, 1/2]; 2^f by a degree-3
 // polynomial fitted here for minimum relative error on [-1/2, 1/2] (max 7.5e-5, i.e. about
-// 1/50 of a bf16 ulp); 2^n applied by adding n to the exponent field. Needs x <= 127; x
-// is clamped below at -125 so that the result stays a normal float (2^-125 stands for 0).
+// 1/50 of a bf16 ulp); 2^n applied by adding n to the exponent field. Meant for x <= 127
+// (larger x give meaningless values, which callers only produce for entries they zero);
+// x is clamped below at -125 so that the result stays a normal float (2^-125 stands for 0).
 __device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
   constexpr float c0 = 0.99992806f, c1 = 0.69326097f, c2 = 0.24261113f, c3 = 0.05517167f;
   constexpr float magic = 12582912.0f;  // 1.5 * 2^23

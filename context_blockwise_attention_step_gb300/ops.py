@@ -288,6 +288,17 @@ def profile_events(start=None, stop=None) -> None:
     check(lib().ra_profile_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event)))
 
 
+def profile_split_event(mid=None) -> None:
+    """Record torch.cuda.Event ``mid`` between the two passes of the next ring_attn_bwd
+    calls (None switches it off)."""
+    if mid is None:
+        check(lib().ra_profile_split_event(None))
+        return
+    if mid.cuda_event == 0:
+        mid.record()
+    check(lib().ra_profile_split_event(ctypes.c_void_p(mid.cuda_event)))
+
+
 def last_error() -> str:
     return lib().ra_last_error().decode()
 

@@ -232,11 +232,17 @@ int ra_test_wait_timeout(uint64_t timeout_ns, void* stream);
 int ra_test_exp2_poly(const float* x, float* y, int n, void* stream);
 
 /* Profiling hook: while set (non-NULL), ra_ring_attn_fwd and ra_ring_attn_bwd record
- * `start_event` immediately before and `stop_event` immediately after their main kernel
- * (the fused forward, or the backward's K/V-tile kernel) on the call's stream, so a caller
- * can time that kernel alone with cudaEventElapsedTime. Both are cudaEvent_t handles owned
- * by the caller; pass NULL, NULL to switch the hook off. Per calling thread. */
+ * `start_event` immediately before and `stop_event` immediately after their main kernels
+ * (the fused forward; the backward's K/V-tile pass and query-tile dq pass, or its single
+ * pass) on the call's stream, so a caller can time them alone with cudaEventElapsedTime.
+ * Both are cudaEvent_t handles owned by the caller; pass NULL, NULL to switch the hook off.
+ * Per calling thread. */
 int ra_profile_events(void* start_event, void* stop_event);
+
+/* Companion of ra_profile_events: while set (non-NULL), the two-pass backward records
+ * `mid_event` between its K/V-tile pass and its dq pass. NULL switches it off. Per
+ * calling thread. */
+int ra_profile_split_event(void* mid_event);
 
 /* Thread-local message describing the last error of this thread ("" if none). */
 const char* ra_last_error(void);
