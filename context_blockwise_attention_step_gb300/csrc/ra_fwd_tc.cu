@@ -331,17 +331,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // pass 1: row max over the visible columns
           float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tS + c * 32, r);
-            if (full) {
+          for (int c2 = 0; c2 < 4; c2 += 2) {  // two chunks in flight per wait
+            uint32_t r2[2][32];
+            tmem_ld32_nowait(tS + c2 * 32, r2[0]);
+            tmem_ld32_nowait(tS + c2 * 32 + 32, r2[1]);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                mx = max3(mx, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            } else {
+            for (int h = 0; h < 2; ++h) {
+              const int c = c2 + h;
+              if (full) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                mx = fmaxf(mx, (c * 32 + i < cnt) ? __uint_as_float(r[i]) : -INFINITY);
+                for (int i = 0; i < 16; ++i)
+                  mx = max3(mx, __uint_as_float(r2[h][2 * i]), __uint_as_float(r2[h][2 * i + 1]));
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  mx = fmaxf(mx, (c * 32 + i < cnt) ? __uint_as_float(r2[h][i]) : -INFINITY);
+              }
             }
           }
           mx *= sl2;
