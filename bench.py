@@ -37,7 +37,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, with the sha256 prefix
 # of the kernel source they were taken on (a changed kernel reports null until re-measured).
-TRAFFIC = {}
+TRAFFIC = {
+    ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
+        {"bytes": 385510747136 + 546531584, "source_sha": "b22e86183dec8db3"},
+    ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
+        {"bytes": 195067297536 + 1264968448, "source_sha": "7b05c7deba8b6174"},
+    ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
+        {"bytes": 13629191424 + 1065236736, "source_sha": "e70d4448c6296156"},
+    ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
+        {"bytes": 3256961792 + 2109121792, "source_sha": "4fcf37257bb4e387"},
+}
 
 
 def parse_args():
@@ -52,6 +61,9 @@ def parse_args():
                     help="target CPU time of one oracle sample")
     ap.add_argument("--secondary", type=int, default=1,
                     help="also time the unfused per-step path and the deterministic backward")
+    ap.add_argument("--once", action="store_true",
+                    help="run the forward, the backward and the merge once each on the "
+                         "workload and exit (a short command to put under a profiler)")
     return ap.parse_args()
 
 
@@ -226,6 +238,18 @@ def run_ours(args, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)
     ws = torch.empty(max(ra.workspace_bytes(prob), 1), device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream(dev)
+    if args.once:
+        ra.ring_attn_fwd(qs, ks, vs, prob, out=out, lse=lse)
+        ra.ring_attn_bwd(dos, qs, ks, vs, out, lse, prob, dq=dq, dk=dk, dv=dv, workspace=ws)
+        mo = torch.zeros(qs.shape, device=dev, dtype=torch.float32)
+        ml = torch.full(lse.shape, float("-inf"), device=dev, dtype=torch.float32)
+        ra.update_out_and_lse(mo, ml, out, lse, prob)
+        torch.cuda.synchronize(dev)
+        status = ra.check_device_status()
+        if status != 0:
+            raise RuntimeError(f"device status: {ra.last_error()}")
+        print(json.dumps({"once": w.name, "status": status}), flush=True)
+        return None
     in_bytes = sum(x.numel() * x.element_size() for x in (qs, ks, vs, dos))
     flush = None if in_bytes > 2 * L2_BYTES else torch.empty(2 * L2_BYTES // 4, device=dev)
 
