@@ -8,10 +8,10 @@
 //
 //   S = Q K^T          tcgen05.mma, Q and K tiles TMA-loaded into 128B-swizzled smem,
 //                      S (128 x 128 f32) accumulated in TMEM
-//   online softmax     one thread per query row reads its S row from TMEM, masks the
-//                      columns beyond its key count, updates the running max m and
-//                      denominator l (registers), writes P = 2^(S*scale*log2e - m) as bf16
-//                      back into TMEM over the consumed S columns
+//   online softmax     two threads per query row (64 columns each) read the S row from
+//                      TMEM, mask the columns beyond the key count, update the running max
+//                      m and denominator l, write P = 2^(S*scale*log2e - m) as bf16 back
+//                      into TMEM over consumed S columns
 //   O += P V           tcgen05.mma with A = P from TMEM, B = V tile (MN-major) from smem
 //
 // The running (m, l, O) persists across all tiles and all ring steps of the block, which
@@ -23,10 +23,13 @@
 // approximation). Finally out = O / l (bf16, or f32 for block outputs) and lse (natural
 // log, f32) are written; a row that saw no key gets out = 0, lse = -inf.
 //
-// Warp roles (384 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 4-7 = softmax of query tile 0, warps 8-11 = softmax of query tile 1. The two
-// softmax warpgroups ping-pong: the MMA order S0(n) S1(n) | O0(n) S0(n+1) O1(n) S1(n+1) | ...
-// lets one tile's softmax run while the tensor core works on the other tile.
+// Warp roles (640 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 4-11 = softmax of query tile 0, warps 12-19 = softmax of query tile 1. Each tile's
+// rows are split between two warpgroups of 64 key columns, which exchange their partial
+// row maxima every K/V tile and their partial sums at the end through shared memory; P
+// goes to S columns [32, 96), each half on its own S columns. The two tiles ping-pong: the
+// MMA order S0(n) S1(n) | O0(n) S0(n+1) O1(n) S1(n+1) | ... lets one tile's softmax run
+// while the tensor core works on the other tile.
 #include <cuda_runtime.h>
 
 #include "ra_internal.h"
@@ -39,12 +42,7 @@ static __device__ unsigned int g_status_fwd;
 
 namespace {
 
-constexpr int kFwdThreads = 384;
-// Of every 8 pairs of softmax exponentials, this many are evaluated on the FMA pipe
-// (exp2_poly2) and the rest on the MUFU unit.
-#ifndef RA_FWD_POLY_PAIRS
-#define RA_FWD_POLY_PAIRS 0
-#endif
+constexpr int kFwdThreads = 640;  // 4 control warps + 4 softmax warpgroups (2 per query tile)
 constexpr int kSubBytes = 128 * 128;  // 128 rows x 64 bf16: one 128B-swizzled sub-tile
 
 template <int DH>
@@ -68,8 +66,11 @@ struct FwdShared {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drain;
+  uint64_t xmax_bar[2][2], xl_bar[2];  // half-row exchanges: [tile][slot], [tile]
   uint32_t tmem_base;
   int abort_flag;
+  float xmax[2][2][2][128];  // [tile][slot][half][row]: partial row maxima
+  float xl[2][2][128];       // [tile][half][row]: partial row sums
 };
 
 // Total K/V tiles a forward item walks, and its first/last valid query rows.
@@ -141,9 +142,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sh.s_full[t], 1);
-      mbar_init(&sh.p_full[t], 128);
+      mbar_init(&sh.p_full[t], 256);
       mbar_init(&sh.o_done[t], 1);
-      mbar_init(&sh.o_free[t], 128);
+      mbar_init(&sh.o_free[t], 256);
+      mbar_init(&sh.xmax_bar[t][0], 256);
+      mbar_init(&sh.xmax_bar[t][1], 256);
+      mbar_init(&sh.xl_bar[t], 256);
     }
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const uint32_t va = sV + st * C::kTileBytes;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 8 * k,
+            mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + 32 + 8 * k,
                    sdesc_sw128(va + k * 2048, kSubBytes, 1024), idO, (n > 0 || k > 0) ? 1u : 0u);
           if (n == N - 1) tc_commit(&sh.o_done[t]);
           if (t == nt - 1) tc_commit(&sh.v_empty[st]);
@@ -282,15 +286,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int t = (warp - 4) >> 2;
+    // Query tile t = (warp - 4) / 8; its rows are split in two halves of 64 key columns
+    // (hf), each held by one warpgroup; the halves exchange partial maxima per tile and
+    // partial sums at the end through shared memory (bounded mbarrier waits).
+    const int t = (warp - 4) >> 3;
+    const int hf = ((warp - 4) >> 2) & 1;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
+    const int c0 = hf * 64;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::col_s(t);
     const uint32_t tO = tmem + lane_off + C::col_o(t);
     const float sl2 = P.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
-    uint32_t s_phase = 0, od_phase = 0;
+    uint32_t s_phase = 0, od_phase = 0, xl_phase = 0;
+    uint32_t xm_phase[2] = {0, 0};
+    int xn = 0;  // max exchanges done (slot = xn & 1)
     for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
       const FwdItem it = decode_fwd(P, w);
       const FwdWalk wk = fwd_walk(P, it);
@@ -308,8 +319,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-          for (int c = 0; c < DH / 32; ++c) store_row32<OutT>(orow_ptr + c * 32, z);
-          *lse_ptr = -INFINITY;
+          for (int c = 0; c < DH / 64; ++c) store_row32<OutT>(orow_ptr + hf * (DH / 2) + c * 32, z);
+          if (hf == 0) *lse_ptr = -INFINITY;
         }
         continue;
       }
@@ -328,17 +339,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           int cnt = lim + 1 - b * kKvTileRows;
           cnt = cnt < 0 ? 0 : (cnt > kKvTileRows ? kKvTileRows : cnt);
           const bool full = __all_sync(0xffffffffu, cnt == kKvTileRows);  // no mask needed
-          // pass 1: row max over the visible columns
+          // pass 1: partial row max over this half's visible columns, then both halves'
           float mx = -INFINITY;
-#pragma unroll
-          for (int c2 = 0; c2 < 4; c2 += 2) {  // two chunks in flight per wait
+          {
             uint32_t r2[2][32];
-            tmem_ld32_nowait(tS + c2 * 32, r2[0]);
-            tmem_ld32_nowait(tS + c2 * 32 + 32, r2[1]);
+            tmem_ld32_nowait(tS + c0, r2[0]);
+            tmem_ld32_nowait(tS + c0 + 32, r2[1]);
             tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int c = c2 + h;
+              const int cs = c0 + 32 * h;
               if (full) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -346,58 +356,62 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                  mx = fmaxf(mx, (c * 32 + i < cnt) ? __uint_as_float(r2[h][i]) : -INFINITY);
+                  mx = fmaxf(mx, (cs + i < cnt) ? __uint_as_float(r2[h][i]) : -INFINITY);
               }
             }
+          }
+          {
+            const int slot = xn & 1;
+            sh.xmax[t][slot][hf][row] = mx;
+            mbar_arrive(&sh.xmax_bar[t][slot]);
+            if (!(ok = mbar_wait(&sh.xmax_bar[t][slot], xm_phase[slot], abort_flag, tmo, status))) break;
+            xm_phase[slot] ^= 1;
+            mx = fmaxf(mx, sh.xmax[t][slot][hf ^ 1][row]);
+            ++xn;
           }
           mx *= sl2;
           const float m_new = fmaxf(m, mx);
           const bool grow = m_new > m + 8.f;  // also true for the first visible key
           const bool need = grow && n > 0 && m != -INFINITY;
-          if (__any_sync(0xffffffffu, need)) {
+          if (__any_sync(0xffffffffu, need)) {  // rescale this half's output columns
             const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll
-            for (int c = 0; c < DH / 32; ++c) {
+            for (int c = 0; c < DH / 64; ++c) {
               uint32_t r[32];
-              tmem_ld32(tO + c * 32, r);
+              tmem_ld32(tO + hf * (DH / 2) + c * 32, r);
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(tO + c * 32, r);
+              tmem_st32(tO + hf * (DH / 2) + c * 32, r);
             }
             if (need) l *= alpha;
           }
           if (grow) m = m_new;
           const float mref = (m == -INFINITY) ? 0.f : m;
-          // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs over the consumed S columns.
-          // RA_FWD_POLY_PAIRS pairs in eight take 2^x from the FMA pipe (exp2_poly2), the
-          // rest from the MUFU unit, so that neither unit limits the tile rate.
+          // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs into S columns [32 + c0/2, +32),
+          // inside this half's own S columns, on a chunk already read (hence the order).
           const uint64_t nm2 = f2(-mref, -mref);
           uint64_t l2 = f2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int ch = hf == 0 ? 1 - k2 : k2;
+            const int cs = c0 + 32 * ch;
             uint32_t r[32], pk[16];
-            tmem_ld32(tS + c * 32, r);
+            tmem_ld32(tS + cs, r);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const uint64_t x = fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, nm2);
-              uint64_t p2;
-              if ((i & 7) < RA_FWD_POLY_PAIRS) {
-                p2 = exp2_poly2(x);
-              } else {
-                const float2 e = f2_split(x);
-                p2 = f2(ex2(e.x), ex2(e.y));
-              }
+              const float2 e = f2_split(x);
+              uint64_t p2 = f2(ex2(e.x), ex2(e.y));
               if (!full) {
-                const int col = c * 32 + 2 * i;
                 float2 pv = f2_split(p2);
-                if (col >= cnt) pv.x = 0.f;
-                if (col + 1 >= cnt) pv.y = 0.f;
+                if (cs + 2 * i >= cnt) pv.x = 0.f;
+                if (cs + 2 * i + 1 >= cnt) pv.y = 0.f;
                 p2 = f2(pv.x, pv.y);
               }
               l2 = add2(l2, p2);
               pk[i] = bf16x2_of(p2);
             }
-            tmem_st16(tS + c * 16, pk);
+            tmem_st16(tS + 32 + c0 / 2 + 16 * ch, pk);
           }
           {
             const float2 ls = f2_split(l2);
@@ -409,21 +423,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
       if (!ok) break;
-      // epilogue: out = O / l, lse = (m + log2 l) * ln 2
+      // epilogue: both halves' sums, out = O / l for this half's columns, lse
+      sh.xl[t][hf][row] = l;
+      mbar_arrive(&sh.xl_bar[t]);
+      if (!mbar_wait(&sh.xl_bar[t], xl_phase, abort_flag, tmo, status)) break;
+      xl_phase ^= 1;
+      l += sh.xl[t][hf ^ 1][row];
       if (!mbar_wait(&sh.o_done[t], od_phase, abort_flag, tmo, status)) break;
       od_phase ^= 1;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int c = 0; c < DH / 64; ++c) {
         uint32_t r[32];
-        tmem_ld32(tO + c * 32, r);
+        tmem_ld32(tO + hf * (DH / 2) + c * 32, r);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv_l;
-        if (valid) store_row32<OutT>(orow_ptr + c * 32, v);
+        if (valid) store_row32<OutT>(orow_ptr + hf * (DH / 2) + c * 32, v);
       }
-      if (valid) *lse_ptr = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+      if (valid && hf == 0) *lse_ptr = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       mbar_arrive(&sh.o_free[t]);
     }
