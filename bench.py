@@ -35,13 +35,13 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, with the sha256 prefix
-# of the kernel source they were taken on (a changed kernel reports null until re-measured).
+# DRAM bytes per launch from an ncu capture, with the hash of the kernel source (and the
+# shared headers) they were taken on: a changed kernel reports null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
         {"bytes": 385510747136 + 546531584, "source_sha": "b22e86183dec8db3"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 195067297536 + 1264968448, "source_sha": "7b05c7deba8b6174"},
+        {"bytes": 281903907072 + 2002203648, "source_sha": "262a4e0b4de0213c"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
         {"bytes": 13629191424 + 1065236736, "source_sha": "e70d4448c6296156"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
@@ -206,9 +206,14 @@ class ClockSampler:
 # ------------------------------------------------------------------------ our arm
 
 def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "context_blockwise_attention_step_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a kernel's source file together with the headers every kernel
+    shares (launch plan, layouts, PTX wrappers)."""
+    csrc = os.path.join(ROOT, "context_blockwise_attention_step_gb300", "csrc")
+    h = hashlib.sha256()
+    for part in (name, "ra_plan.h", "ra_layout.h", "ra_ptx.cuh"):
+        with open(os.path.join(csrc, part), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def run_ours(args, rank, world, local_rank):
