@@ -14,8 +14,8 @@
 //   S  = Q K^T                 tcgen05 (SS), TMEM (two buffers)
 //   P  = 2^(S*scale*log2e - lse*log2e)   one thread per query row, masked by key counts
 //   dP = dO V^T                tcgen05 (SS), TMEM
-//   dS = P * (dP - delta)      bf16, written over the S buffer
-//   dQ += dS K                 tcgen05 (TS: dS from TMEM, K MN-major), f32 in TMEM
+//   dS = P * (dP - delta)      bf16, written to a 128B-swizzled smem tile
+//   dQ += dS K                 tcgen05 (SS: dS K-major, K MN-major), f32 in TMEM
 //
 // MMA order: S(0) dP(0) S(1) | dQ(0) dP(1) S(2) | dQ(1) dP(2) S(3) | ... so the next
 // tile's S is ready while the current dS is computed. Warp roles (384 threads): warp 0
@@ -50,7 +50,8 @@ struct DqCfg {
   static constexpr int kOffDO = kTileBytes;
   static constexpr int kOffK = 2 * kTileBytes;                // 2 stages
   static constexpr int kOffV = kOffK + 2 * kTileBytes;        // 2 stages
-  static constexpr int kOffBar = kOffV + 2 * kTileBytes;
+  static constexpr int kOffDS = kOffV + 2 * kTileBytes;       // dS [query][key] bf16, 32 KB
+  static constexpr int kOffBar = kOffDS + 2 * kSubBytes;
   static constexpr int kSmemBytes = kOffBar + 256;
   static constexpr int kKSteps = DH / 16;
   static constexpr uint32_t kTmemCols = 512;
@@ -204,7 +205,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t ds_phase[2] = {0, 0};
       int kc = 0;
       const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A and B K-major
-      const uint32_t idQ = idesc_bf16_f32(128, DH, 0, 1);   // dQ: A from TMEM, B MN-major
+      const uint32_t idQ = idesc_bf16_f32(128, DH, 0, 1);   // dQ: A K-major, B MN-major
+      const uint32_t sDS = smem_u32(smem + C::kOffDS);
       const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       bool ok = true;
@@ -257,11 +259,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           ds_phase[n & 1] ^= 1;
           tc_fence_after();
           const uint32_t ka = sK + st * C::kTileBytes;
-          const uint32_t tds = tmem + (n & 1 ? C::kColS1 : C::kColS0) + 32;
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::kColDQ, tds + 8 * k, sdesc_sw128(ka + k * 2048, kSubBytes, 1024), idQ,
-                   (n > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + off, 16, 1024),
+                   sdesc_sw128(ka + k * 2048, kSubBytes, 1024), idQ, (n > 0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(&sh.k_empty[st]);
           if (n + 1 < N) ok = issue_dP(n + 1);
           if (ok && n + 2 < N) ok = issue_S(n + 2);
@@ -281,6 +284,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const int c0 = wg * 64;               // this warpgroup's key columns
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // this thread's row of the dS tile: sub-tile wg (keys c0 .. c0+63), 128 bytes
+    uint8_t* ds_row = smem + C::kOffDS + wg * kSubBytes + row * 128;
     const float sl2 = P.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
     uint32_t s_phase[2] = {0, 0}, dp_phase = 0, dd_phase = 0;
@@ -381,10 +386,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
               x = mul2(x, f2_of_bf16x2(pp[16 * ch + i]));
               o[i] = bf16x2_of(x);
             }
-            // dS (bf16) into columns [32, 96) of the S buffer: the A operand of dQ += dS K
-            tmem_st16(tS + 32 + c0 / 2 + 16 * ch, o);
+            // dS (bf16) into the swizzled smem tile: the A operand of dQ += dS K. The previous
+            // dQ MMA, the last reader of the tile, completed before dP (dp_full) was signalled.
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int chunk = 4 * ch + q;
+              uint4 v4;
+              v4.x = o[4 * q + 0];
+              v4.y = o[4 * q + 1];
+              v4.z = o[4 * q + 2];
+              v4.w = o[4 * q + 3];
+              *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = v4;
+            }
           }
-          tmem_st_wait();
+          fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(&sh.ds_full[buf]);
         }

@@ -15,8 +15,8 @@
 //   dP^T = V dO^T                tcgen05 (SS), TMEM buffer Y
 //   dV  += P^T dO                tcgen05 (TS: P^T from X), f32 in TMEM for the whole walk
 //   dS^T = P^T * (dP^T - delta)  delta = rowsum(dO * O) from the preprocess kernel; bf16,
-//                                written to Y (over the consumed dP^T) and to smem
-//   dK  += dS^T Q                tcgen05 (TS: dS^T from Y), f32 in TMEM for the whole walk
+//                                written to a 128B-swizzled smem tile
+//   dK  += dS^T Q                tcgen05 (SS: dS^T K-major), f32 in TMEM for the whole walk
 //   dQ   = dS K                  tcgen05 (SS, dS read MN-major from smem) into Y, then
 //                                added with vector float reductions into f32 dq sums
 //
@@ -180,9 +180,10 @@ __device__ __forceinline__ void transpose8_f4(uint32_t (&r)[32], int t) {
 }
 
 // dS^T = P^T * (dP^T - delta) for the 32 query columns [c0 + 32*CH, +32) of this thread's
-// K/V row, from their dP^T registers: the bf16 result goes to Y columns
-// [32 + c0/2 + 16*CH, +16) (the A operand of the dK MMA) and, when dQ is computed, to the
-// 128B-swizzled smem tile (the A operand of the dQ MMA).
+// K/V row, from their dP^T registers: the bf16 result goes to the 128B-swizzled smem tile
+// [K/V row][query], the A operand of the dK MMA (K-major) and of the dQ MMA (MN-major).
+// (Kept out of TMEM: MMAs that read an operand from TMEM slow down while the softmax
+// warps load and store TMEM.)
 template <int CH, bool kWithDQ>
 __device__ __forceinline__ void ds_from(const uint32_t (&dp)[32], uint32_t tY, int c0, const float* dl,
                                         const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
@@ -195,23 +196,19 @@ __device__ __forceinline__ void ds_from(const uint32_t (&dp)[32], uint32_t tY, i
     x = mul2(x, f2_of_bf16x2(pp[16 * CH + i]));
     o[i] = bf16x2_of(x);
   }
-  tmem_st16(tY + 32 + c0 / 2 + 16 * CH, o);
-  if constexpr (kWithDQ) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int chunk = 4 * CH + q;
-      uint4 v;
-      v.x = o[4 * q + 0];
-      v.y = o[4 * q + 1];
-      v.z = o[4 * q + 2];
-      v.w = o[4 * q + 3];
-      *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = v;
-    }
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = 4 * CH + q;
+    uint4 v;
+    v.x = o[4 * q + 0];
+    v.y = o[4 * q + 1];
+    v.z = o[4 * q + 2];
+    v.w = o[4 * q + 3];
+    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = v;
   }
 }
 
-// One chunk at a time (the output lands on dP^T columns this thread has already read, so the
-// chunk order differs between the two warpgroups).
+// One chunk at a time.
 template <int CH, bool kWithDQ>
 __device__ __forceinline__ void ds_chunk(uint32_t tY, int c0, const float* dl,
                                          const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
@@ -410,9 +407,11 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
               tc_fence_after();
               const uint32_t sQp = sQ0 + ((qi - 1) & 1) * C::kStageBytes;
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQp + k * 2048, kSubBytes, 1024),
-                       idKV, (i > 1 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+                mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                       sdesc_sw128(sQp + k * 2048, kSubBytes, 1024), idKV, (i > 1 || k > 0) ? 1u : 0u);
+              }
               tc_commit(&sh.q_empty[(qi - 1) & 1]);
             }
 #pragma unroll
@@ -444,9 +443,11 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
             tc_fence_after();
             const uint32_t sQl = sQ0 + (ql & 1) * C::kStageBytes;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQl + k * 2048, kSubBytes, 1024),
-                     idKV, (wk.N > 1 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+              mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                     sdesc_sw128(sQl + k * 2048, kSubBytes, 1024), idKV, (wk.N > 1 || k > 0) ? 1u : 0u);
+            }
             tc_commit(&sh.q_empty[ql & 1]);
           }
           if (!ok) break;
@@ -489,14 +490,16 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
             tc_fence_after();
             issue_S(sQ0 + st1 * C::kStageBytes);
           }
-          // dK += dS^T Q (dS^T from Y) ; dQ = dS K into Y
+          // dK += dS^T Q ; dQ = dS K into Y (dS^T from smem, K-major / MN-major)
           if (!mbar_wait(&sh.ds_full, ds_phase, abort_flag, tmo, status)) return false;
           ds_phase ^= 1;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ts(tmem + C::kColDK, tY + 32 + 8 * k, sdesc_sw128(sQ + k * 2048, kSubBytes, 1024), idKV,
-                   (i > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
+            mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                   sdesc_sw128(sQ + k * 2048, kSubBytes, 1024), idKV, (i > 0 || k > 0) ? 1u : 0u);
+          }
           if constexpr (kWithDQ) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -634,8 +637,7 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
         }
         mbar_arrive(&sh.ls_empty[slot]);
         ++t;
-        tmem_st_wait();
-        if constexpr (kWithDQ) fence_proxy_async_smem();
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sh.ds_full);
         return true;
