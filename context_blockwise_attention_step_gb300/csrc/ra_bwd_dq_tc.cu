@@ -347,26 +347,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const int cs = c0 + 32 * ch;
             const uint32_t (&sv)[32] = sv2[ch];
             const bool full = __all_sync(0xffffffffu, cnt >= cs + 32);
+            // staged: every FMA, then every exponential, then masking and packing
+            uint64_t xv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              xv[i] = fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, nl2);
+            float ev[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint64_t x =
-                  fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2, nl2);
-              float p0, p1;
-              if ((i & 7) < RA_DQ_POLY_PAIRS) {  // visible entries have x <= 0
-                const float2 e = f2_split(exp2_poly2(x));
-                p0 = e.x;
-                p1 = e.y;
-              } else {
-                const float2 e = f2_split(x);
-                p0 = ex2(e.x);
-                p1 = ex2(e.y);
-              }
-              if (!full) {
-                if (cs + 2 * i >= cnt) p0 = 0.f;
-                if (cs + 2 * i + 1 >= cnt) p1 = 0.f;
-              }
-              pp[16 * ch + i] = pack_bf16x2(p0, p1);
+              const float2 e = f2_split((i & 7) < RA_DQ_POLY_PAIRS ? exp2_poly2(xv[i]) : xv[i]);
+              ev[2 * i] = (i & 7) < RA_DQ_POLY_PAIRS ? e.x : ex2(e.x);  // poly: x <= 0 if visible
+              ev[2 * i + 1] = (i & 7) < RA_DQ_POLY_PAIRS ? e.y : ex2(e.y);
             }
+            if (!full) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (cs + i >= cnt) ev[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pp[16 * ch + i] = pack_bf16x2(ev[2 * i], ev[2 * i + 1]);
           }
           if (!(ok = mbar_wait(&sh.dp_full, dp_phase, abort_flag, tmo, status))) break;
           dp_phase ^= 1;
@@ -380,12 +379,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             const int cs = c0 + 32 * ch;
             const uint32_t (&dp)[32] = dp2[ch];
             uint32_t o[16];
+            uint64_t xv[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              uint64_t x = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), dl2);
-              x = mul2(x, f2_of_bf16x2(pp[16 * ch + i]));
-              o[i] = bf16x2_of(x);
-            }
+            for (int i = 0; i < 16; ++i)
+              xv[i] = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), dl2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xv[i] = mul2(xv[i], f2_of_bf16x2(pp[16 * ch + i]));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = bf16x2_of(xv[i]);
             // dS (bf16) into the swizzled smem tile: the A operand of dQ += dS K. The previous
             // dQ MMA, the last reader of the tile, completed before dP (dp_full) was signalled.
 #pragma unroll

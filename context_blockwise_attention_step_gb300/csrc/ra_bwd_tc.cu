@@ -189,13 +189,16 @@ __device__ __forceinline__ void ds_from(const uint32_t (&dp)[32], uint32_t tY, i
                                         const uint32_t (&pp)[32], uint8_t* ds_row, int row) {
   const int cs = c0 + 32 * CH;
   uint32_t o[16];
+  uint64_t xv[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 d2 = *reinterpret_cast<const float2*>(dl + cs + 2 * i);
-    uint64_t x = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), f2(d2.x, d2.y));
-    x = mul2(x, f2_of_bf16x2(pp[16 * CH + i]));
-    o[i] = bf16x2_of(x);
+    xv[i] = sub2(f2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), f2(d2.x, d2.y));
   }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) xv[i] = mul2(xv[i], f2_of_bf16x2(pp[16 * CH + i]));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = bf16x2_of(xv[i]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int chunk = 4 * CH + q;
@@ -228,26 +231,29 @@ __device__ __forceinline__ void p_from(const uint32_t (&sv)[32], uint32_t tX, in
   const int cs = c0 + 32 * CH;
   uint32_t pk[16];
   const bool full = __all_sync(0xffffffffu, lo <= cs);
+  // staged: every FMA, then every exponential, then masking and packing
+  uint64_t xv[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float2 n2 = *reinterpret_cast<const float2*>(nl + cs + 2 * i);
-    const uint64_t x = fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2,
-                            f2(n2.x, n2.y));
-    float p0, p1;
-    if ((i & 7) < RA_BWD_POLY_PAIRS) {  // visible entries have x <= 0; hidden ones are zeroed
-      const float2 e = f2_split(exp2_poly2(x));
-      p0 = e.x;
-      p1 = e.y;
-    } else {
-      const float2 e = f2_split(x);
-      p0 = ex2(e.x);
-      p1 = ex2(e.y);
-    }
-    if (!full) {
-      if (cs + 2 * i < lo) p0 = 0.f;
-      if (cs + 2 * i + 1 < lo) p1 = 0.f;
-    }
-    pk[i] = pack_bf16x2(p0, p1);
+    xv[i] = fma2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sl2x2,
+                 f2(n2.x, n2.y));
+  }
+  float ev[32];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // poly: visible entries have x <= 0; hidden ones are zeroed
+    const float2 e = f2_split((i & 7) < RA_BWD_POLY_PAIRS ? exp2_poly2(xv[i]) : xv[i]);
+    ev[2 * i] = (i & 7) < RA_BWD_POLY_PAIRS ? e.x : ex2(e.x);
+    ev[2 * i + 1] = (i & 7) < RA_BWD_POLY_PAIRS ? e.y : ex2(e.y);
+  }
+  if (!full) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (cs + i < lo) ev[i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    pk[i] = pack_bf16x2(ev[2 * i], ev[2 * i + 1]);
     pp[16 * CH + i] = pk[i];
   }
   tmem_st16(tX + 32 + c0 / 2 + 16 * CH, pk);

@@ -340,25 +340,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           cnt = cnt < 0 ? 0 : (cnt > kKvTileRows ? kKvTileRows : cnt);
           const bool full = __all_sync(0xffffffffu, cnt == kKvTileRows);  // no mask needed
           // pass 1: partial row max over this half's visible columns, then both halves'
-          float mx = -INFINITY;
-          {
-            uint32_t r2[2][32];
-            tmem_ld32_nowait(tS + c0, r2[0]);
-            tmem_ld32_nowait(tS + c0 + 32, r2[1]);
-            tmem_wait_ld();
+          uint32_t r2[2][32];
+          tmem_ld32_nowait(tS + c0, r2[0]);
+          tmem_ld32_nowait(tS + c0 + 32, r2[1]);
+          tmem_wait_ld();
+          float mx;
+          {  // four independent max chains (one chain of 32 dependent max ops is slow)
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int cs = c0 + 32 * h;
-              if (full) {
+              for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  mx = max3(mx, __uint_as_float(r2[h][2 * i]), __uint_as_float(r2[h][2 * i + 1]));
-              } else {
+                for (int i = 0; i < 32; i += 4) {
+                  mq[2 * h] = max3(mq[2 * h], __uint_as_float(r2[h][i]), __uint_as_float(r2[h][i + 1]));
+                  mq[2 * h + 1] =
+                      max3(mq[2 * h + 1], __uint_as_float(r2[h][i + 2]), __uint_as_float(r2[h][i + 3]));
+                }
+            } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  mx = fmaxf(mx, (cs + i < cnt) ? __uint_as_float(r2[h][i]) : -INFINITY);
-              }
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float v = (c0 + 32 * h + i < cnt) ? __uint_as_float(r2[h][i]) : -INFINITY;
+                  mq[2 * h + (i & 1)] = fmaxf(mq[2 * h + (i & 1)], v);
+                }
             }
+            mx = fmaxf(max3(mq[0], mq[1], mq[2]), mq[3]);
           }
           {
             const int slot = xn & 1;
@@ -397,20 +404,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int cs = c0 + 32 * ch;
             uint32_t r[32], pk[16];
             tmem_ld32(tS + cs, r);
+            // staged: every FMA, then every exponential (independent, so they issue back to
+            // back), then packing and two partial sums
+            uint64_t xv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              xv[i] = fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, nm2);
+            float ev[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint64_t x = fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, nm2);
-              const float2 e = f2_split(x);
-              uint64_t p2 = f2(ex2(e.x), ex2(e.y));
-              if (!full) {
-                float2 pv = f2_split(p2);
-                if (cs + 2 * i >= cnt) pv.x = 0.f;
-                if (cs + 2 * i + 1 >= cnt) pv.y = 0.f;
-                p2 = f2(pv.x, pv.y);
-              }
-              l2 = add2(l2, p2);
+              const float2 e = f2_split(xv[i]);
+              ev[2 * i] = ex2(e.x);
+              ev[2 * i + 1] = ex2(e.y);
+            }
+            if (!full) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (cs + i >= cnt) ev[i] = 0.f;
+            }
+            uint64_t la = f2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t p2 = f2(ev[2 * i], ev[2 * i + 1]);
+              if (i & 1) la = add2(la, p2); else l2 = add2(l2, p2);
               pk[i] = bf16x2_of(p2);
             }
+            l2 = add2(l2, la);
             tmem_st16(tS + 32 + c0 / 2 + 16 * ch, pk);
           }
           {
