@@ -398,12 +398,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // inside this half's own S columns, on a chunk already read (hence the order).
           const uint64_t nm2 = f2(-mref, -mref);
           uint64_t l2 = f2(0.f, 0.f);
+          uint32_t rr[2][32];
+          tmem_ld32_nowait(tS + c0, rr[0]);
+          tmem_ld32_nowait(tS + c0 + 32, rr[1]);
+          tmem_wait_ld();
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2) {
-            const int ch = hf == 0 ? 1 - k2 : k2;
+          for (int ch = 0; ch < 2; ++ch) {
             const int cs = c0 + 32 * ch;
-            uint32_t r[32], pk[16];
-            tmem_ld32(tS + cs, r);
+            uint32_t (&r)[32] = rr[ch];
+            uint32_t pk[16];
             // staged: every FMA, then every exponential (independent, so they issue back to
             // back), then packing and two partial sums
             uint64_t xv[16];
