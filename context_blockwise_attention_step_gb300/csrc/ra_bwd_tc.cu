@@ -74,7 +74,7 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[2], do_full[2], q_empty[2];  // Q and dO of a stage land separately
   uint64_t ls_full[2], ls_empty[2];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
   uint64_t acc_done, drain;
@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     mbar_init(&sh.kv_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.q_full[i], 1);
+      mbar_init(&sh.do_full[i], 1);
       mbar_init(&sh.q_empty[i], 1);
       mbar_init(&sh.ls_full[i], 32);
       mbar_init(&sh.ls_empty[i], 256);
@@ -352,13 +353,16 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
           const int st = qcount & 1;
           const uint32_t ph = (qcount >> 1) & 1;
           if (!mbar_wait(&sh.q_empty[st], ph ^ 1, abort_flag, tmo, status)) return false;
-          mbar_expect_tx(&sh.q_full[st], 2 * C::kTileBytes);
+          // Q first, on its own barrier: S of this tile needs only Q, and is issued well
+          // before dP needs dO
           const int qrow = sd.row_off + r * P.shard_stride + q0;
           uint8_t* base = smem + C::kOffQ + st * C::kStageBytes;
-          for (int d = 0; d < C::kSub; ++d) {
+          mbar_expect_tx(&sh.q_full[st], C::kTileBytes);
+          for (int d = 0; d < C::kSub; ++d)
             tma_load_3d(base + d * kSubBytes, &tmQ, &sh.q_full[st], d * 64, h, qrow);
-            tma_load_3d(base + C::kTileBytes + d * kSubBytes, &tmDO, &sh.q_full[st], d * 64, h, qrow);
-          }
+          mbar_expect_tx(&sh.do_full[st], C::kTileBytes);
+          for (int d = 0; d < C::kSub; ++d)
+            tma_load_3d(base + C::kTileBytes + d * kSubBytes, &tmDO, &sh.do_full[st], d * 64, h, qrow);
           ++qcount;
           return true;
         });
@@ -420,6 +424,8 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
               }
               tc_commit(&sh.q_empty[(qi - 1) & 1]);
             }
+            if (!mbar_wait(&sh.do_full[st], (qi >> 1) & 1, abort_flag, tmo, status)) return false;
+            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < C::kKSteps; ++k) {
               const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
@@ -469,6 +475,7 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
           // dV += P^T dO (P^T from X columns [32, 96)). dV is overwritten at the first tile:
           // the previous item's dK / dV were read by the P / dS threads before they
           // signalled P(0).
+          if (!mbar_wait(&sh.do_full[st], (qi >> 1) & 1, abort_flag, tmo, status)) return false;
           if (!mbar_wait(&sh.p_full, p_phase, abort_flag, tmo, status)) return false;
           p_phase ^= 1;
           tc_fence_after();
@@ -672,8 +679,7 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
   } else if (warp >= 12) {
     // ------------------------------------------------------------------ dQ warpgroup
     if constexpr (kWithDQ) {
-      const int quarter = warp & 3;
-      const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
+      const int quarter = warp & 3;  // TMEM lanes = query rows quarter*32 .. +31
       const uint32_t tQ = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColY;
       const float mul = P.dq_mul;
       uint32_t dqf_phase = 0;
