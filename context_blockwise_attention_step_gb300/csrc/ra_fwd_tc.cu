@@ -395,7 +395,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (grow) m = m_new;
           const float mref = (m == -INFINITY) ? 0.f : m;
           // pass 2: P = 2^(S*scale*log2e - m) as bf16 pairs into S columns [32 + c0/2, +32),
-          // inside this half's own S columns, on a chunk already read (hence the order).
+          // inside this half's own S columns; both chunks are in registers before any P is
+          // written.
           const uint64_t nm2 = f2(-mref, -mref);
           uint64_t l2 = f2(0.f, 0.f);
           uint32_t rr[2][32];
