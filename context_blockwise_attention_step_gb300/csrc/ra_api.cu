@@ -168,6 +168,19 @@ Plan* make_plan(const ra_problem* p, int which, int step_begin, int step_end, in
   }
   P->n_seqs = ns;
   P->n_items = items;
+  // Walk order of the backward items: K/V tiles innermost when one K/V head group's Q and
+  // dO of the longest sequence (all ranks) are larger than this device's L2.
+  if (which == 1 && n > 0) {
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) == cudaSuccess && l2 > 0) {
+      const int64_t elem = p->dtype == RA_F32 ? 4 : 2;
+      const int64_t group_qdo = len[order[0]] * P->group * p->head_dim * elem * 2;
+      P->bwd_kt_inner = group_qdo > static_cast<int64_t>(l2) ? 1 : 0;
+    } else {
+      cudaGetLastError();  // no device: keep the default order
+    }
+  }
   return P;
 }
 

@@ -39,6 +39,7 @@ struct Plan {
   int32_t kv_shard_only;         // backward, >= 0: only this K/V shard's tiles are items
   int32_t out_f32;               // forward output stored as float32 (else problem dtype)
   int32_t bwd_accum;             // backward: add float32 gradients into the outputs
+  int32_t bwd_kt_inner;          // backward items: K/V tiles innermost (see decode_bwd)
   float scale, scale_log2;
   float dq_mul;                  // factor on dS K before it is added to the dq sums
   uint64_t timeout_ns;
@@ -104,20 +105,31 @@ RA_HD FwdItem decode_fwd(const Plan& P, int w) {
 }
 
 // Backward decode: K/V heads outermost, so that the CTAs running at the same time share
-// one K/V head and therefore add into the same query heads' dq rows (which then stay in
-// L2); within a head, K/V tiles in increasing order (early keys are seen by the most
-// queries), shards innermost.
+// one K/V head and therefore the same query heads' Q, dO (and dq rows). Within a head,
+// either K/V tiles in increasing order (early keys are seen by the most queries) with the
+// shards innermost, or, when one K/V head group's Q and dO are larger than the L2
+// (bwd_kt_inner), shards in order with the K/V tiles innermost: the CTAs running together
+// then hold neighbouring tiles of one shard, whose walks visit nearly the same query tiles
+// in the same order, so each Q / dO tile is read from DRAM about once per pass of that
+// group instead of once per CTA. (Measured on GB300: 3 % faster K/V pass at 131072 tokens,
+// 32/8 heads; 3-5 % slower where the group's Q and dO fit in L2.)
 RA_HD BwdItem decode_bwd(const Plan& P, int w) {
   BwdItem it;
   it.seq = find_seq(P, w);
   const SeqDesc& s = P.seq[it.seq];
   const int ns = plan_kv_shards(P);
-  const int per_head = ceil_div(s.L, kKvTileRows) * ns;
+  const int nkt = ceil_div(s.L, kKvTileRows);
+  const int per_head = nkt * ns;
   int x = w - s.item_start;
   it.hk = x / per_head;
   x %= per_head;
-  it.j = P.kv_shard_only >= 0 ? P.kv_shard_only : x % ns;
-  it.kt = x / ns;
+  if (P.bwd_kt_inner) {
+    it.kt = x % nkt;
+    it.j = P.kv_shard_only >= 0 ? P.kv_shard_only : x / nkt;
+  } else {
+    it.j = P.kv_shard_only >= 0 ? P.kv_shard_only : x % ns;
+    it.kt = x / ns;
+  }
   return it;
 }
 
