@@ -35,17 +35,18 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch from an ncu capture, with the hash of the kernel source (and the
-# shared headers) they were taken on: a changed kernel reports null until re-measured.
+# DRAM bytes per launch from an ncu capture, with the hash of the kernel source (with the
+# shared headers and the plan construction) they were taken on: a changed kernel reports
+# null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 385510747136 + 546531584, "source_sha": "b22e86183dec8db3"},
+        {"bytes": 105359756544 + 545768192, "source_sha": "6296841165a41dcf"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 281903907072 + 2002203648, "source_sha": "262a4e0b4de0213c"},
+        {"bytes": 177917911296 + 1260479744, "source_sha": "4c9682df32a5584b"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 13629191424 + 1065236736, "source_sha": "e70d4448c6296156"},
+        {"bytes": 15281313280 + 1071060480, "source_sha": "0650b34ace70bf0f"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3256961792 + 2109121792, "source_sha": "4fcf37257bb4e387"},
+        {"bytes": 3256780288 + 2109334528, "source_sha": "bc07f5a76275cf1b"},
 }
 
 
@@ -207,10 +208,10 @@ class ClockSampler:
 
 def kernel_source_hash(name: str) -> str:
     """sha256 prefix of a kernel's source file together with the headers every kernel
-    shares (launch plan, layouts, PTX wrappers)."""
+    shares (launch plan, layouts, PTX wrappers) and the plan construction (item order)."""
     csrc = os.path.join(ROOT, "context_blockwise_attention_step_gb300", "csrc")
     h = hashlib.sha256()
-    for part in (name, "ra_plan.h", "ra_layout.h", "ra_ptx.cuh"):
+    for part in (name, "ra_plan.h", "ra_layout.h", "ra_ptx.cuh", "ra_api.cu"):
         with open(os.path.join(csrc, part), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
