@@ -44,7 +44,7 @@ TRAFFIC = {
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
         {"bytes": 177917911296 + 1260479744, "source_sha": "4c9682df32a5584b"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 15281313280 + 1071060480, "source_sha": "0650b34ace70bf0f"},
+        {"bytes": 31715411456 + 1066704640, "source_sha": "8bcf7b7a819e45e0"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
         {"bytes": 3256780288 + 2109334528, "source_sha": "bc07f5a76275cf1b"},
 }

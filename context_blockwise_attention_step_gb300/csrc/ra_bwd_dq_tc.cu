@@ -14,13 +14,16 @@
 //   S  = Q K^T                 tcgen05 (SS), TMEM (two buffers)
 //   P  = 2^(S*scale*log2e - lse*log2e)   one thread per query row, masked by key counts
 //   dP = dO V^T                tcgen05 (SS), TMEM
-//   dS = P * (dP - delta)      bf16, written to a 128B-swizzled smem tile
-//   dQ += dS K                 tcgen05 (SS: dS K-major, K MN-major), f32 in TMEM
+//   dS = P * (dP - delta)      bf16, written over the tile's S buffer (columns [32, 96))
+//   dQ += dS K                 tcgen05 (TS: dS from TMEM, K MN-major), f32 in TMEM
 //
-// MMA order: S(0) dP(0) S(1) | dQ(0) dP(1) S(2) | dQ(1) dP(2) S(3) | ... so the next
-// tile's S is ready while the current dS is computed. Warp roles (384 threads): warp 0
-// TMA producer, warp 1 TMEM allocator + MMA issuer, warps 4-7 and 8-11 the P / dS
-// warpgroups (thread = query row; key columns 0-63 and 64-127; they also write dq).
+// MMA order: S(0) dP(0) S(1) | dP(1) dQ(0) S(2) | dP(2) dQ(1) S(3) | ...: once dS(n) is
+// written, dP(n+1) goes first, so the softmax threads compute dS(n+1) (into the other S
+// buffer) while dQ(n) runs, and S(n+2) is ready while dS(n+1) is computed. K stays in
+// shared memory from S(n) to dQ(n), which now trails dP(n+1): three K stages let the load
+// of K(n+2) start before dQ(n) ends. Warp roles (384 threads): warp 0 TMA producer, warp 1
+// TMEM allocator + MMA issuer, warps 4-7 and 8-11 the P / dS warpgroups (thread = query
+// row; key columns 0-63 and 64-127; they also write dq).
 #include <cuda_runtime.h>
 
 #include "ra_internal.h"
@@ -48,10 +51,10 @@ struct DqCfg {
   static constexpr int kTileBytes = 128 * DH * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTileBytes;
-  static constexpr int kOffK = 2 * kTileBytes;                // 2 stages
-  static constexpr int kOffV = kOffK + 2 * kTileBytes;        // 2 stages
-  static constexpr int kOffDS = kOffV + 2 * kTileBytes;       // dS [query][key] bf16, 32 KB
-  static constexpr int kOffBar = kOffDS + 2 * kSubBytes;
+  static constexpr int kKStages = 3;  // K is held from S(n) to dQ(n), which trails dP(n+1)
+  static constexpr int kOffK = 2 * kTileBytes;                // kKStages stages
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes; // 2 stages
+  static constexpr int kOffBar = kOffV + 2 * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 256;
   static constexpr int kKSteps = DH / 16;
   static constexpr uint32_t kTmemCols = 512;
@@ -61,7 +64,7 @@ struct DqCfg {
 
 struct DqBars {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], dp_full, ds_full[2], dq_done, dq_free;
   uint64_t drain;
   uint32_t tmem_base;
@@ -124,9 +127,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(&sh.k_full[i], 1);
       mbar_init(&sh.k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.v_full[i], 1);
       mbar_init(&sh.v_empty[i], 1);
       mbar_init(&sh.s_full[i], 1);
@@ -183,10 +188,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           for (int b = 0; b < nb; ++b, ++kc) {
             const int st = kc & 1;
             const uint32_t ph = (kc >> 1) & 1;
-            if (!(ok = mbar_wait(&sh.k_empty[st], ph ^ 1, abort_flag, tmo, status))) break;
-            mbar_expect_tx(&sh.k_full[st], C::kTileBytes);
+            const int kst = kc % C::kKStages;
+            const uint32_t kph = (kc / C::kKStages) & 1;
+            if (!(ok = mbar_wait(&sh.k_empty[kst], kph ^ 1, abort_flag, tmo, status))) break;
+            mbar_expect_tx(&sh.k_full[kst], C::kTileBytes);
             for (int d = 0; d < C::kSub; ++d)
-              tma_load_3d(smem + C::kOffK + st * C::kTileBytes + d * kSubBytes, &tmK, &sh.k_full[st],
+              tma_load_3d(smem + C::kOffK + kst * C::kTileBytes + d * kSubBytes, &tmK, &sh.k_full[kst],
                           d * 64, hk, krow + b * kKvTileRows);
             if (!(ok = mbar_wait(&sh.v_empty[st], ph ^ 1, abort_flag, tmo, status))) break;
             mbar_expect_tx(&sh.v_full[st], C::kTileBytes);
@@ -205,8 +212,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t ds_phase[2] = {0, 0};
       int kc = 0;
       const uint32_t idS = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A and B K-major
-      const uint32_t idQ = idesc_bf16_f32(128, DH, 0, 1);   // dQ: A K-major, B MN-major
-      const uint32_t sDS = smem_u32(smem + C::kOffDS);
+      const uint32_t idQ = idesc_bf16_f32(128, DH, 0, 1);   // dQ: A from TMEM, B MN-major
       const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       bool ok = true;
@@ -218,8 +224,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         q_phase ^= 1;
         tc_fence_after();
         auto issue_S = [&](int n) -> bool {
-          const int c = kc + n, st = c & 1;
-          if (!mbar_wait(&sh.k_full[st], (c >> 1) & 1, abort_flag, tmo, status)) return false;
+          const int c = kc + n, st = c % C::kKStages;
+          if (!mbar_wait(&sh.k_full[st], (c / C::kKStages) & 1, abort_flag, tmo, status)) return false;
           tc_fence_after();
           const uint32_t ka = sK + st * C::kTileBytes;
 #pragma unroll
@@ -254,20 +260,21 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tc_fence_after();
         }
         for (int n = 0; n < N && ok; ++n) {
-          const int c = kc + n, st = c & 1;
+          const int c = kc + n, st = c % C::kKStages;
           if (!(ok = mbar_wait(&sh.ds_full[n & 1], ds_phase[n & 1], abort_flag, tmo, status))) break;
           ds_phase[n & 1] ^= 1;
           tc_fence_after();
+          // dP(n+1) first: dP(n) has been read (ds_full), and dS(n+1) goes to the other S
+          // buffer, so the softmax threads can compute it while dQ(n) runs
+          if (n + 1 < N && !(ok = issue_dP(n + 1))) break;
           const uint32_t ka = sK + st * C::kTileBytes;
+          const uint32_t tds = tmem + (n & 1 ? C::kColS1 : C::kColS0) + 32;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * kSubBytes + (k & 3) * 32;
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + off, 16, 1024),
-                   sdesc_sw128(ka + k * 2048, kSubBytes, 1024), idQ, (n > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tmem + C::kColDQ, tds + 8 * k, sdesc_sw128(ka + k * 2048, kSubBytes, 1024), idQ,
+                   (n > 0 || k > 0) ? 1u : 0u);
           tc_commit(&sh.k_empty[st]);
-          if (n + 1 < N) ok = issue_dP(n + 1);
-          if (ok && n + 2 < N) ok = issue_S(n + 2);
+          if (n + 2 < N) ok = issue_S(n + 2);
         }
         if (!ok) break;
         tc_commit(&sh.dq_done);
@@ -284,8 +291,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = quarter * 32 + lane;  // query row within the tile = TMEM lane
     const int c0 = wg * 64;               // this warpgroup's key columns
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // this thread's row of the dS tile: sub-tile wg (keys c0 .. c0+63), 128 bytes
-    uint8_t* ds_row = smem + C::kOffDS + wg * kSubBytes + row * 128;
     const float sl2 = P.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
     uint32_t s_phase[2] = {0, 0}, dp_phase = 0, dd_phase = 0;
@@ -376,7 +381,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int ch = 0; ch < 2; ++ch) {
-            const int cs = c0 + 32 * ch;
             const uint32_t (&dp)[32] = dp2[ch];
             uint32_t o[16];
             uint64_t xv[16];
@@ -387,20 +391,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             for (int i = 0; i < 16; ++i) xv[i] = mul2(xv[i], f2_of_bf16x2(pp[16 * ch + i]));
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = bf16x2_of(xv[i]);
-            // dS (bf16) into the swizzled smem tile: the A operand of dQ += dS K. The previous
-            // dQ MMA, the last reader of the tile, completed before dP (dp_full) was signalled.
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int chunk = 4 * ch + q;
-              uint4 v4;
-              v4.x = o[4 * q + 0];
-              v4.y = o[4 * q + 1];
-              v4.z = o[4 * q + 2];
-              v4.w = o[4 * q + 3];
-              *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) = v4;
-            }
+            // dS (bf16) into columns [32, 96) of this tile's S buffer (read into registers
+            // above): the A operand of dQ += dS K
+            tmem_st16(tS + 32 + c0 / 2 + 16 * ch, o);
           }
-          fence_proxy_async_smem();
+          tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&sh.ds_full[buf]);
         }
