@@ -300,18 +300,42 @@ def run_ours(args, rank, world, local_rank):
     dev_nat = [torch.empty_like(x) for x in nat]
     dev_out_nat = [torch.empty_like(t) for t in (out, lse, dq, dk, dv)]
 
+    copy_stream = torch.cuda.Stream(dev)
+
     def e2e_step():
-        for h, d in zip(host, dev_nat):
-            d.copy_(h, non_blocking=True)
-        sm = [ra.shard_tokens(x, prob) for x in dev_nat]
+        # Copies run on their own stream, overlapped with the kernels: q, k, v first (the
+        # forward needs them), dO during the forward, out and lse back during the backward,
+        # dq, dk, dv back at the end. The step ends when the last copy has landed.
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            for h, d in zip(host[:3], dev_nat[:3]):
+                d.copy_(h, non_blocking=True)
+            qkv_in = torch.cuda.Event()
+            qkv_in.record(copy_stream)
+            dev_nat[3].copy_(host[3], non_blocking=True)
+            do_in = torch.cuda.Event()
+            do_in.record(copy_stream)
+        stream.wait_event(qkv_in)
+        sm = [ra.shard_tokens(x, prob) for x in dev_nat[:3]]
         o, l = ra.ring_attn_fwd(sm[0], sm[1], sm[2], prob)
-        g = ra.ring_attn_bwd(sm[3], sm[0], sm[1], sm[2], o, l, prob, workspace=ws)
         ra.unshard_tokens(o, prob, out=dev_out_nat[0])
         ra.unshard_lse(l, prob, out=dev_out_nat[1])
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(stream)
+        stream.wait_event(do_in)
+        sdo = ra.shard_tokens(dev_nat[3], prob)
+        g = ra.ring_attn_bwd(sdo, sm[0], sm[1], sm[2], o, l, prob, workspace=ws)
+        copy_stream.wait_event(fwd_done)
+        with torch.cuda.stream(copy_stream):
+            for d, h in zip(dev_out_nat[:2], outs_h[:2]):
+                h.copy_(d, non_blocking=True)
         for t, d in zip(g, dev_out_nat[2:]):
             ra.unshard_tokens(t, prob, out=d)
-        for d, h in zip(dev_out_nat, outs_h):
-            h.copy_(d, non_blocking=True)
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            for d, h in zip(dev_out_nat[2:], outs_h[2:]):
+                h.copy_(d, non_blocking=True)
+        stream.wait_stream(copy_stream)
 
     e2e_step()
     torch.cuda.synchronize(dev)

@@ -363,7 +363,15 @@ int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, co
   PlanHolder E(make_plan(p, 2, step, step + 1, r_only, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  if (use_tc(p)) {
+  if (use_tc(p) && !fused_bwd(p)) {
+    // the two passes of the deterministic backward, restricted to (rank, step), adding into
+    // the float32 sums: dk, dv from the K/V-tile kernel, dq from the query-tile kernel
+    PlanHolder P(make_plan(p, 1, step, step + 1, r_only, 0, nullptr, kv_only));
+    P.p->bwd_accum = 1;
+    e = ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvAccum, q, k, v, dout, lse, delta, nullptr, dk_acc,
+                          dv_acc, st);
+    if (e == cudaSuccess) e = ra::launch_bwd_dq_tc(*P.p, q, k, v, dout, lse, delta, dq_acc, st);
+  } else if (use_tc(p)) {
     PlanHolder P(make_plan(p, 1, step, step + 1, r_only, 0, nullptr, kv_only));
     P.p->bwd_accum = 1;
     e = ra::launch_bwd_tc(*P.p, ra::BwdKind::kBlockAccum, q, k, v, dout, lse, delta, dq_acc, dk_acc,

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                           const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ CUtensorMap tmDO, const __grid_constant__ Plan P,
                           const float* __restrict__ lse, const float* __restrict__ delta,
-                          __nv_bfloat16* __restrict__ dq) {
+                          void* __restrict__ dq) {
   using C = DqCfg<DH>;
   extern __shared__ __align__(1024) uint8_t smem[];
   DqBars& sh = *reinterpret_cast<DqBars*>(smem + C::kOffBar);
@@ -302,12 +302,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const bool valid = a < L;
       const size_t qrow = static_cast<size_t>(sd.row_off + it.r * P.shard_stride + a);
       const int N = dq_walk_tiles(P, it, L);
-      if (N == 0) {  // no key visible: dq = 0
-        if (valid) {
-          uint32_t z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
-          __nv_bfloat16* dst = dq + (qrow * P.hq + it.h) * DH;
+      if (N == 0) {  // no key visible: dq = 0 (nothing to add for bwd_accum)
+        if (valid && !P.bwd_accum) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(dq) + (qrow * P.hq + it.h) * DH;
 #pragma unroll
           for (int c = wg * DH / 64; c < (wg + 1) * DH / 64; ++c) {
             uint4* d = reinterpret_cast<uint4*>(dst + c * 32);
@@ -401,17 +398,31 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
       }
       if (!ok) break;
-      // dq = scale * dQ: warpgroup 0 writes columns [0, DH/2), warpgroup 1 the rest
+      // dq = scale * dQ (or dq += scale * dQ into float32 sums for bwd_accum, the per-step
+      // block backward): warpgroup 0 takes columns [0, DH/2), warpgroup 1 the rest
       if (!mbar_wait(&sh.dq_done, dd_phase, abort_flag, tmo, status)) break;
       dd_phase ^= 1;
       tc_fence_after();
-      __nv_bfloat16* dst = dq + (qrow * P.hq + it.h) * DH;
+      const size_t qoff = (qrow * P.hq + it.h) * DH;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(dq) + qoff;
+      float* dst_acc = static_cast<float*>(dq) + qoff;
 #pragma unroll
       for (int c = 0; c < DH / 64; ++c) {
         const int col = wg * (DH / 2) + 32 * c;
         uint32_t rr[32];
         tmem_ld32(tmem + lane_off + C::kColDQ + col, rr);
-        if (valid) {
+        if (valid && P.bwd_accum) {
+          float4* d = reinterpret_cast<float4*>(dst_acc + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 u = d[q];
+            u.x += __uint_as_float(rr[4 * q + 0]) * P.scale;
+            u.y += __uint_as_float(rr[4 * q + 1]) * P.scale;
+            u.z += __uint_as_float(rr[4 * q + 2]) * P.scale;
+            u.w += __uint_as_float(rr[4 * q + 3]) * P.scale;
+            d[q] = u;
+          }
+        } else if (valid) {
           uint4* d = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -447,8 +458,7 @@ cudaError_t launch_one(const Plan& P, const CUtensorMap& mq, const CUtensorMap& 
                                        C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = n_items < n_sm ? n_items : n_sm;
-  kern<<<grid, kDqThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta,
-                                                static_cast<__nv_bfloat16*>(dq));
+  kern<<<grid, kDqThreads, C::kSmemBytes, st>>>(mq, mk, mv, mdo, P, lse, delta, dq);
   return cudaGetLastError();
 }
 

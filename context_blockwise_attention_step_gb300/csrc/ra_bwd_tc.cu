@@ -779,6 +779,8 @@ cudaError_t launch_bwd_tc(const Plan& P, BwdKind kind, const void* q, const void
       return launch_dh<false, false>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
     case BwdKind::kBlockAccum:
       return launch_dh<true, true>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
+    case BwdKind::kKvAccum:
+      return launch_dh<false, true>(P, mq, mk, mv, mdo, lse, delta, dq_acc, dk, dv, n_sm, st);
   }
   return cudaErrorInvalidValue;
 }

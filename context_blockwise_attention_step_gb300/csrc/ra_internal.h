@@ -22,7 +22,7 @@ cudaError_t launch_fwd_tc(const Plan& P, const void* q, const void* k, const voi
 // Backward K/V-tile kernel variants: kFused (dq sums into dq_acc, dk / dv stored in the
 // problem dtype), kKvOnly (dk / dv only; dq_acc unused), kBlockAccum (float32 dq, dk, dv
 // added into the outputs).
-enum class BwdKind { kFused, kKvOnly, kBlockAccum };
+enum class BwdKind { kFused, kKvOnly, kBlockAccum, kKvAccum };
 cudaError_t launch_bwd_tc(const Plan& P, BwdKind kind, const void* q, const void* k, const void* v,
                           const void* dout, const float* lse, const float* delta, float* dq_acc,
                           void* dk, void* dv, cudaStream_t st);

@@ -38,8 +38,11 @@ long max_len(const Plan& P) {
 // one piece per lane), and lane 0 writes the merged lse only after the broadcast, so no
 // lane can read an already-merged lse. The row's out / block loads are issued before the
 // broadcast so that their latency overlaps the lse loads'.
+// At most 32 registers (8 blocks of 256 threads per SM), so that 64 warps per SM have their
+// loads in flight: measured on GB300 at 131072 tokens, 32 heads, 5.2 against 4.7 TB/s with
+// the 33 registers the compiler picks unbounded (48 warps).
 template <typename BT, int VEC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
     merge_kernel(const __grid_constant__ Plan P, float* __restrict__ out, float* __restrict__ lse,
                  const BT* __restrict__ bout, const float* __restrict__ blse) {
   const SeqDesc& sd = P.seq[blockIdx.y];

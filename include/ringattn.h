@@ -154,7 +154,10 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
  * Inputs as for ra_ring_attn_bwd (out, lse: the final forward results). The workspace
  * (device, >= ra_workspace_bytes(p, 2), 256-byte aligned) receives the per-row
  * dot(dout, out) of the selected rank(s); it is overwritten. Rows outside the selection are
- * not touched. Calls must not overlap on the GPU when they add into the same rows. */
+ * not touched. Calls must not overlap on the GPU when they add into the same rows. The bf16
+ * path runs the two atomic-free passes of ra_ring_attn_bwd restricted to the step (each
+ * accumulator row is added by one thread), so results are run-to-run bit-identical;
+ * RA_BWD=fused selects the single pass that adds block_dq with float reductions. */
 int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, const void* k,
                       const void* v, const void* out, const float* lse, const void* dout,
                       float* dq_acc, float* dk_acc, float* dv_acc, void* workspace,

@@ -241,7 +241,8 @@ def _shard_major_inputs(w):
 def test_block_backward_per_step_matches_oracle(w):
     """ra_block_attn_bwd of every step (all ranks), each added into zeroed float32
     accumulators, equals the oracle's per-step terms of the ring backward; the sum over the
-    steps equals the fused backward."""
+    steps equals the fused backward. The block backward has no atomics: a repeated call
+    gives the same bits."""
     prob, (qs, ks, vs, dos), (q_h, k_h, v_h, do_h), rows = _shard_major_inputs(w)
     out_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, prob)
     o_h = packed(out_s.float().cpu().numpy()).astype(np.float64)
@@ -255,6 +256,11 @@ def test_block_backward_per_step_matches_oracle(w):
                          w.varlen, steps=[s])
         for name, a, r_ in zip(("dq", "dk", "dv"), acc, ref):
             assert_grad(w, f"{name} step {s}", packed(a.cpu().numpy()), r_)
+        if s == w.D - 1:
+            again = [torch.zeros(t.shape, device="cuda") for t in (qs, ks, vs)]
+            ra.block_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob, -1, s, *again)
+            for name, a, b in zip(("dq", "dk", "dv"), acc, again):
+                assert torch.equal(a, b), f"{name} step {s}: repeated call differs"
         for t, a in zip(tot, acc):
             t += a
     fused = ra.ring_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob)
@@ -339,10 +345,23 @@ def test_fma_pipe_exp2_error_bound():
 
 @pytest.mark.parametrize("w", [SMALL[0], SMALL[7], SMALL[10]], ids=lambda w: w.name)
 def test_fused_backward_variant_matches_oracle(w, monkeypatch):
-    """The single-pass backward with float reductions for dq (RA_BWD=fused) stays correct:
-    it is the kernel the per-step block backward runs on."""
+    """The single-pass backward with float reductions for dq (RA_BWD=fused) stays correct,
+    for the whole ring and for the per-step block backward it then also runs."""
     monkeypatch.setenv("RA_BWD", "fused")
     res, inputs = run(w)
     out, lse, grads = oracle(w, inputs)
     for name, ref in zip(("dq", "dk", "dv"), grads):
         assert_grad(w, name, res[name], ref)
+    prob, (qs, ks, vs, dos), (q_h, k_h, v_h, do_h), rows = _shard_major_inputs(w)
+    out_s, lse_s = ra.ring_attn_fwd(qs, ks, vs, prob)
+    o_h = packed(out_s.float().cpu().numpy()).astype(np.float64)
+    l_h = lse_s.cpu().numpy().astype(np.float64)
+    l_h = l_h if w.varlen else l_h.transpose(1, 0, 2).reshape(w.hq, -1)
+    s = w.D - 1
+    acc = [torch.zeros(t.shape, device="cuda") for t in (qs, ks, vs)]
+    ra.block_attn_bwd(dos, qs, ks, vs, out_s, lse_s, prob, -1, s, *acc)
+    ref = R.ring_bwd(q_h, k_h, v_h, o_h, l_h, do_h, w.lengths, w.D, w.layout, w.causal,
+                     w.varlen, steps=[s])
+    for name, a, r_ in zip(("dq", "dk", "dv"), acc, ref):
+        assert_grad(w, f"block {name} step {s}", packed(a.cpu().numpy()), r_)
+    assert ra.check_device_status() == 0, ra.last_error()
