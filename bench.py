@@ -40,13 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 105359756544 + 545768192, "source_sha": "6296841165a41dcf"},
+        {"bytes": 106431422464 + 546876672, "source_sha": "d555b17ea4190bc0"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 177917911296 + 1260479744, "source_sha": "4c9682df32a5584b"},
+        {"bytes": 182788549888 + 1262106112, "source_sha": "623baec631c5abe0"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 31715411456 + 1066704640, "source_sha": "8bcf7b7a819e45e0"},
+        {"bytes": 25589536512 + 1065758208, "source_sha": "714dfd5e5d721544"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3256780288 + 2109334528, "source_sha": "bc07f5a76275cf1b"},
+        {"bytes": 3255460352 + 2109253120, "source_sha": "39d52e761dae73ef"},
 }
 
 
