@@ -214,6 +214,9 @@ size_t delta_bytes(const ra_problem* p) {
   return align256(size_t(rows) * p->hq * sizeof(float));
 }
 
+// The K/V-tile pass's shared item counter (dynamic scheduling), one 256-byte block.
+size_t sched_bytes(const ra_problem* p) { return use_tc(p) ? 256 : 0; }
+
 size_t dq_acc_bytes(const ra_problem* p) {
   if (!fused_bwd(p)) return 0;
   int64_t rows = 0;
@@ -292,7 +295,7 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
 
 size_t ra_workspace_bytes(const ra_problem* p, int which) {
   if (validate(p) != RA_OK) return 0;
-  if (which == 1) return delta_bytes(p) + dq_acc_bytes(p);
+  if (which == 1) return delta_bytes(p) + dq_acc_bytes(p) + sched_bytes(p);
   if (which == 2) return delta_bytes(p);
   return 0;
 }
@@ -303,7 +306,7 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
   if (int e = validate(p)) return e;
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv)
     return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
-  const size_t need = delta_bytes(p) + dq_acc_bytes(p);
+  const size_t need = delta_bytes(p) + dq_acc_bytes(p) + sched_bytes(p);
   if (workspace_bytes < need)
     return fail(RA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (need > 0 && (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256))
@@ -313,9 +316,17 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
   PlanHolder E(make_plan(p, 2, 0, p->D, -1, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  int32_t* counter = nullptr;  // the K/V-tile pass takes its items from this counter
+  if (use_tc(p)) {
+    counter = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + delta_bytes(p) +
+                                         dq_acc_bytes(p));
+    e = cudaMemsetAsync(counter, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "item counter clear");
+  }
   if (use_tc(p) && !fused_bwd(p)) {
     // dk, dv from the K/V-tile kernel without its dq part; dq query-tile-major
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
+    P.p->work_counter = counter;
     e = profiled(st, [&] {
       cudaError_t r = ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvOnly, q, k, v, dout, lse, delta, nullptr,
                                         dk, dv, st);
@@ -329,6 +340,7 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
     e = cudaMemsetAsync(dq_acc, 0, dq_acc_bytes(p), st);
     if (e != cudaSuccess) return cuda_fail(e, "dq workspace clear");
     PlanHolder P(make_plan(p, 1, 0, p->D, -1, 0));
+    P.p->work_counter = counter;
     e = profiled(st, [&] {
       return ra::launch_bwd_tc(*P.p, ra::BwdKind::kFused, q, k, v, dout, lse, delta, dq_acc, dk, dv, st);
     });

@@ -66,7 +66,7 @@ struct BwdCfg {
   static constexpr int kOffDS = kOffQ + 2 * kStageBytes;     // 128 x 128 bf16
   static constexpr int kOffLs = kOffDS + 2 * kSubBytes;      // [2 slots][-lse*log2e | delta][128]
   static constexpr int kOffBar = kOffLs + 2 * 2 * 128 * 4;
-  static constexpr int kSmemBytes = kOffBar + 192;
+  static constexpr int kSmemBytes = kOffBar + 256;
   static constexpr int kKSteps = DH / 16;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColDK = 0, kColDV = DH, kColX = 2 * DH, kColY = 2 * DH + 128;
@@ -78,10 +78,12 @@ struct BwdBars {
   uint64_t ls_full[2], ls_empty[2];
   uint64_t s_full, p_full, dp_full, ds_full, dq_full, dq_free;
   uint64_t acc_done, drain;
+  uint64_t item_full[2], item_empty[2];  // the CTA's item queue
+  int item[2];
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(BwdBars) <= 192, "barrier block");
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
 static_assert(BwdCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 
 struct BwdWalk {
@@ -274,6 +276,31 @@ __device__ __forceinline__ void p_chunk(uint32_t tX, int c0, const float* nl, ui
 template <bool kWithDQ>
 constexpr int bwd_threads() { return kWithDQ ? 512 : 384; }
 
+// The CTA's item queue (two slots). The producer thread takes the next item, from the shared
+// counter when there is one (dynamic: a CTA that finishes early takes more items, in index
+// order, so the CTAs running together still hold neighbouring items), else by the static
+// stride, and publishes it; every other role reads it from the ring, so all roles walk the
+// same items. A value >= n_items ends the walk.
+__device__ __forceinline__ int item_publish(BwdBars& sh, const Plan& P, int k,
+                                            volatile int* abort_flag, uint64_t tmo,
+                                            unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, abort_flag, tmo, status)) return -1;
+  const int w = P.work_counter ? atomicAdd(P.work_counter, 1)
+                               : static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x);
+  sh.item[slot] = w;
+  mbar_arrive(&sh.item_full[slot]);
+  return w;
+}
+__device__ __forceinline__ int item_take(BwdBars& sh, int k, volatile int* abort_flag,
+                                         uint64_t tmo, unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_full[slot], (k >> 1) & 1, abort_flag, tmo, status)) return -1;
+  const int w = *reinterpret_cast<volatile int*>(&sh.item[slot]);
+  mbar_arrive(&sh.item_empty[slot]);
+  return w;
+}
+
 template <int DH, bool kWithDQ, bool kAccum>
 __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     ring_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -312,6 +339,10 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 128);
     mbar_init(&sh.acc_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.item_full[i], 1);
+      mbar_init(&sh.item_empty[i], 1 + 32 + 256 + (kWithDQ ? 128 : 0));
+    }
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -336,7 +367,9 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     if (lane == 0) {
       uint32_t kv_phase = 0;
       int qcount = 0;
-      for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+      for (int kq = 0;; ++kq) {
+        const int w = item_publish(sh, P, kq, abort_flag, tmo, status);
+        if (w < 0 || w >= P.n_items) break;
         const BwdItem it = decode_bwd(P, w);
         const BwdWalk wk = bwd_walk(P, it);
         if (wk.N == 0) continue;
@@ -390,7 +423,10 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
         tc_commit(&sh.s_full);
       };
       bool ok = true;
-      for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+      for (int kq = 0; ok; ++kq) {
+        const int w = item_take(sh, kq, abort_flag, tmo, status);
+        if (w < 0) ok = false;
+        if (w < 0 || w >= P.n_items) break;
         const BwdItem it = decode_bwd(P, w);
         const BwdWalk wk = bwd_walk(P, it);
         if (wk.N == 0) continue;
@@ -537,7 +573,9 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     // ------------------------------------------------------------------ lse / delta loader
     float* ls_base = reinterpret_cast<float*>(smem + C::kOffLs);
     int t = 0;
-    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+    for (int kq = 0;; ++kq) {
+      const int w = item_take(sh, kq, abort_flag, tmo, status);
+      if (w < 0 || w >= P.n_items) break;
       const BwdItem it = decode_bwd(P, w);
       const BwdWalk wk = bwd_walk(P, it);
       if (wk.N == 0) continue;
@@ -579,7 +617,9 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
     const uint64_t sl2x2 = f2(P.scale_log2, P.scale_log2);
     uint32_t s_phase = 0, dp_phase = 0, ad_phase = 0;
     int t = 0;
-    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+    for (int kq = 0;; ++kq) {
+      const int w = item_take(sh, kq, abort_flag, tmo, status);
+      if (w < 0 || w >= P.n_items) break;
       const BwdItem it = decode_bwd(P, w);
       const BwdWalk wk = bwd_walk(P, it);
       const SeqDesc& sd = P.seq[it.seq];
@@ -683,7 +723,9 @@ __global__ void __launch_bounds__(bwd_threads<kWithDQ>(), 1)
       const uint32_t tQ = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColY;
       const float mul = P.dq_mul;
       uint32_t dqf_phase = 0;
-      for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+      for (int kq = 0;; ++kq) {
+        const int w = item_take(sh, kq, abort_flag, tmo, status);
+        if (w < 0 || w >= P.n_items) break;
         const BwdItem it = decode_bwd(P, w);
         const BwdWalk wk = bwd_walk(P, it);
         if (wk.N == 0) continue;

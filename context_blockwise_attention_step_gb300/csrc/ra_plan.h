@@ -43,6 +43,7 @@ struct Plan {
   float scale, scale_log2;
   float dq_mul;                  // factor on dS K before it is added to the dq sums
   uint64_t timeout_ns;
+  int32_t* work_counter;         // backward K/V pass: shared item counter (null: static stride)
   SeqDesc seq[RA_MAX_SEQS];
 };
 

@@ -135,9 +135,9 @@ size_t ra_workspace_bytes(const ra_problem* p, int which);
  * dk, dv (like k) in the problem dtype; every element is written. The bf16 path runs two
  * passes without atomics (K/V tiles: dk, dv; query tiles: dq), so results are run-to-run
  * bit-identical. The workspace (device, >= ra_workspace_bytes(p, 1), 256-byte aligned)
- * holds the per-row dot(dout, out) (and, only when the environment variable RA_BWD=fused
- * selects the single-pass variant with float reductions, float32 dq sums); it is
- * overwritten. */
+ * holds the per-row dot(dout, out), the counter from which the K/V-tile pass's CTAs take
+ * their work items (and, only when the environment variable RA_BWD=fused selects the
+ * single-pass variant with float reductions, float32 dq sums); it is overwritten. */
 int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const void* v,
                      const void* out, const float* lse, const void* dout, void* dq,
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
