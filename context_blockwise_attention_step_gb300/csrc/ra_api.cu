@@ -214,7 +214,8 @@ size_t delta_bytes(const ra_problem* p) {
   return align256(size_t(rows) * p->hq * sizeof(float));
 }
 
-// The K/V-tile pass's shared item counter (dynamic scheduling), one 256-byte block.
+// The shared item counters of the K/V-tile pass and of the dq pass (dynamic scheduling),
+// one 256-byte block.
 size_t sched_bytes(const ra_problem* p) { return use_tc(p) ? 256 : 0; }
 
 size_t dq_acc_bytes(const ra_problem* p) {
@@ -316,11 +317,11 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
   PlanHolder E(make_plan(p, 2, 0, p->D, -1, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
-  int32_t* counter = nullptr;  // the K/V-tile pass takes its items from this counter
+  int32_t* counter = nullptr;  // the K/V-tile pass takes its items from counter[0], dq from [1]
   if (use_tc(p)) {
     counter = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + delta_bytes(p) +
                                          dq_acc_bytes(p));
-    e = cudaMemsetAsync(counter, 0, sizeof(int32_t), st);
+    e = cudaMemsetAsync(counter, 0, 2 * sizeof(int32_t), st);  // K/V pass, dq pass
     if (e != cudaSuccess) return cuda_fail(e, "item counter clear");
   }
   if (use_tc(p) && !fused_bwd(p)) {

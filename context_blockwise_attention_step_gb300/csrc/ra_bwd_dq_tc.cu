@@ -67,6 +67,8 @@ struct DqBars {
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], dp_full, ds_full[2], dq_done, dq_free;
   uint64_t drain;
+  uint64_t item_full[2], item_empty[2];  // the CTA's item queue
+  int item[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -104,6 +106,29 @@ __device__ __forceinline__ int dq_walk_tiles(const Plan& P, const DqItem& it, in
   return n;
 }
 
+// The CTA's item queue (two slots), as in the K/V-tile pass: the producer thread takes the
+// next item from the shared counter (or by the static stride when there is none) and
+// publishes it; the MMA thread and the softmax threads read it from the ring.
+__device__ __forceinline__ int dq_item_publish(DqBars& sh, const Plan& P, int k,
+                                               volatile int* abort_flag, uint64_t tmo,
+                                               unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, abort_flag, tmo, status)) return -1;
+  const int w = P.work_counter ? atomicAdd(P.work_counter, 1)
+                               : static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x);
+  sh.item[slot] = w;
+  mbar_arrive(&sh.item_full[slot]);
+  return w;
+}
+__device__ __forceinline__ int dq_item_take(DqBars& sh, int k, volatile int* abort_flag,
+                                            uint64_t tmo, unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_full[slot], (k >> 1) & 1, abort_flag, tmo, status)) return -1;
+  const int w = *reinterpret_cast<volatile int*>(&sh.item[slot]);
+  mbar_arrive(&sh.item_empty[slot]);
+  return w;
+}
+
 template <int DH>
 __global__ void __launch_bounds__(kDqThreads, 1)
     ring_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -139,6 +164,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.dq_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.item_full[i], 1);
+      mbar_init(&sh.item_empty[i], 1 + 256);
+    }
     mbar_init(&sh.dq_free, 256);
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
@@ -164,7 +193,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0) {
       uint32_t q_phase = 0;
       int kc = 0;
-      for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+      for (int kq = 0;; ++kq) {
+        const int w = dq_item_publish(sh, P, kq, abort_flag, tmo, status);
+        if (w < 0 || w >= P.n_items) break;
         const DqItem it = decode_dq(P, w);
         const SeqDesc& sd = P.seq[it.seq];
         const int L = sd.L;
@@ -216,7 +247,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const uint32_t sQ = smem_u32(smem + C::kOffQ), sDO = smem_u32(smem + C::kOffDO);
       const uint32_t sK = smem_u32(smem + C::kOffK), sV = smem_u32(smem + C::kOffV);
       bool ok = true;
-      for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+      for (int kq = 0; ok; ++kq) {
+        const int w = dq_item_take(sh, kq, abort_flag, tmo, status);
+        if (w < 0) ok = false;
+        if (w < 0 || w >= P.n_items) break;
         const DqItem it = decode_dq(P, w);
         const int N = dq_walk_tiles(P, it, P.seq[it.seq].L);
         if (N == 0) continue;
@@ -294,7 +328,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float sl2 = P.scale_log2;
     const uint64_t sl2x2 = f2(sl2, sl2);
     uint32_t s_phase[2] = {0, 0}, dp_phase = 0, dd_phase = 0;
-    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+    for (int kq = 0;; ++kq) {
+      const int w = dq_item_take(sh, kq, abort_flag, tmo, status);
+      if (w < 0 || w >= P.n_items) break;
       const DqItem it = decode_dq(P, w);
       const SeqDesc& sd = P.seq[it.seq];
       const int L = sd.L;
@@ -467,7 +503,8 @@ cudaError_t launch_one(const Plan& P, const CUtensorMap& mq, const CUtensorMap& 
 cudaError_t launch_bwd_dq_tc(const Plan& P0, const void* q, const void* k, const void* v,
                              const void* dout, const float* lse, const float* delta, void* dq,
                              cudaStream_t st) {
-  Plan P = P0;  // re-number the items for query tiles
+  Plan P = P0;  // re-number the items for query tiles; the next counter of the block
+  P.work_counter = P0.work_counter ? P0.work_counter + 1 : nullptr;
   int items = 0;
   for (int i = 0; i < P.n_seqs; ++i) {
     P.seq[i].item_start = items;
