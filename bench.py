@@ -40,13 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 106431422464 + 546876672, "source_sha": "d555b17ea4190bc0"},
+        {"bytes": 55270092800 + 542587904, "source_sha": "806b8e97542bda61"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 182788549888 + 1262106112, "source_sha": "623baec631c5abe0"},
+        {"bytes": 182255197952 + 1262697472, "source_sha": "cbca52f2b48729bb"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 25589536512 + 1065758208, "source_sha": "714dfd5e5d721544"},
+        {"bytes": 16185985280 + 1060701184, "source_sha": "392a4bd46866d8aa"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3255460352 + 2109253120, "source_sha": "39d52e761dae73ef"},
+        {"bytes": 3255721216 + 2109176064, "source_sha": "f434c32cda1f5705"},
 }
 
 
