@@ -297,7 +297,7 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
 size_t ra_workspace_bytes(const ra_problem* p, int which) {
   if (validate(p) != RA_OK) return 0;
   if (which == 1) return delta_bytes(p) + dq_acc_bytes(p) + sched_bytes(p);
-  if (which == 2) return delta_bytes(p);
+  if (which == 2) return delta_bytes(p) + sched_bytes(p);
   return 0;
 }
 
@@ -364,7 +364,7 @@ int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, co
     return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
   if (rank >= p->D || rank < -1) return fail(RA_ERR_INVALID_ARG, "rank %d out of range", rank);
   if (step < 0 || step >= p->D) return fail(RA_ERR_INVALID_ARG, "step %d out of range", step);
-  const size_t need = delta_bytes(p);
+  const size_t need = delta_bytes(p) + sched_bytes(p);
   if (workspace_bytes < need)
     return fail(RA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
   if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -376,17 +376,25 @@ int ra_block_attn_bwd(const ra_problem* p, int rank, int step, const void* q, co
   PlanHolder E(make_plan(p, 2, step, step + 1, r_only, 0));
   cudaError_t e = ra::launch_bwd_delta(*E.p, p->dtype, out, dout, delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
+  int32_t* counter = nullptr;  // item counters of the two passes, as in ra_ring_attn_bwd
+  if (use_tc(p)) {
+    counter = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + delta_bytes(p));
+    e = cudaMemsetAsync(counter, 0, 2 * sizeof(int32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "item counter clear");
+  }
   if (use_tc(p) && !fused_bwd(p)) {
     // the two passes of the deterministic backward, restricted to (rank, step), adding into
     // the float32 sums: dk, dv from the K/V-tile kernel, dq from the query-tile kernel
     PlanHolder P(make_plan(p, 1, step, step + 1, r_only, 0, nullptr, kv_only));
     P.p->bwd_accum = 1;
+    P.p->work_counter = counter;
     e = ra::launch_bwd_tc(*P.p, ra::BwdKind::kKvAccum, q, k, v, dout, lse, delta, nullptr, dk_acc,
                           dv_acc, st);
     if (e == cudaSuccess) e = ra::launch_bwd_dq_tc(*P.p, q, k, v, dout, lse, delta, dq_acc, st);
   } else if (use_tc(p)) {
     PlanHolder P(make_plan(p, 1, step, step + 1, r_only, 0, nullptr, kv_only));
     P.p->bwd_accum = 1;
+    P.p->work_counter = counter;
     e = ra::launch_bwd_tc(*P.p, ra::BwdKind::kBlockAccum, q, k, v, dout, lse, delta, dq_acc, dk_acc,
                           dv_acc, st);
   } else {

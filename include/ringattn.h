@@ -153,7 +153,7 @@ int ra_ring_attn_bwd(const ra_problem* p, const void* q, const void* k, const vo
  * Summing the calls of steps 0..D-1 into zeroed accumulators gives the full backward.
  * Inputs as for ra_ring_attn_bwd (out, lse: the final forward results). The workspace
  * (device, >= ra_workspace_bytes(p, 2), 256-byte aligned) receives the per-row
- * dot(dout, out) of the selected rank(s); it is overwritten. Rows outside the selection are
+ * dot(dout, out) of the selected rank(s) and the passes' item counters; it is overwritten. Rows outside the selection are
  * not touched. Calls must not overlap on the GPU when they add into the same rows. The bf16
  * path runs the two atomic-free passes of ra_ring_attn_bwd restricted to the step (each
  * accumulator row is added by one thread), so results are run-to-run bit-identical;
