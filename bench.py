@@ -40,13 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 55270092800 + 542587904, "source_sha": "806b8e97542bda61"},
+        {"bytes": 55073855488 + 541530112, "source_sha": "1dd24d99d75bc66a"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 182255197952 + 1262697472, "source_sha": "cbca52f2b48729bb"},
+        {"bytes": 178724998400 + 1260292864, "source_sha": "256c8cbfa7455492"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 16185985280 + 1060701184, "source_sha": "392a4bd46866d8aa"},
+        {"bytes": 16273171456 + 1060346880, "source_sha": "fbc2bb4cf9f12f00"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3255721216 + 2109176064, "source_sha": "f434c32cda1f5705"},
+        {"bytes": 3256117248 + 2109385216, "source_sha": "416e42caefd976cc"},
 }
 
 
