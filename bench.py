@@ -40,13 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 55073855488 + 541530112, "source_sha": "1dd24d99d75bc66a"},
+        {"bytes": 55127535616 + 542334208, "source_sha": "45c9785223774eaf"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 178724998400 + 1260292864, "source_sha": "256c8cbfa7455492"},
+        {"bytes": 180803717632 + 1260159744, "source_sha": "256c8cbfa7455492"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 16273171456 + 1060346880, "source_sha": "fbc2bb4cf9f12f00"},
+        {"bytes": 16182210048 + 1061005312, "source_sha": "31f2306f1323bf55"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3256117248 + 2109385216, "source_sha": "416e42caefd976cc"},
+        {"bytes": 3256150528 + 2108904704, "source_sha": "416e42caefd976cc"},
 }
 
 

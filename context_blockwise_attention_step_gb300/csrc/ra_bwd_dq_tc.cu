@@ -21,9 +21,11 @@
 // written, dP(n+1) goes first, so the softmax threads compute dS(n+1) (into the other S
 // buffer) while dQ(n) runs, and S(n+2) is ready while dS(n+1) is computed. K stays in
 // shared memory from S(n) to dQ(n), which now trails dP(n+1): three K stages let the load
-// of K(n+2) start before dQ(n) ends. Warp roles (384 threads): warp 0 TMA producer, warp 1
-// TMEM allocator + MMA issuer, warps 4-7 and 8-11 the P / dS warpgroups (thread = query
-// row; key columns 0-63 and 64-127; they also write dq).
+// of K(n+2) start before dQ(n) ends. Items (query tiles) come from a counter in the
+// caller's workspace, passed from the producer thread to the other roles through a two-slot
+// ring in shared memory. Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM
+// allocator + MMA issuer, warps 4-7 and 8-11 the P / dS warpgroups (thread = query row;
+// key columns 0-63 and 64-127; they also write dq).
 #include <cuda_runtime.h>
 
 #include "ra_internal.h"

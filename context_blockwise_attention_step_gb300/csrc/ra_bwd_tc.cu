@@ -20,13 +20,16 @@
 //   dQ   = dS K                  tcgen05 (SS, dS read MN-major from smem) into Y, then
 //                                added with vector float reductions into f32 dq sums
 //
-// The MMA warp issues, per query tile i: dV(i), dP(i), S(i+1), dK(i), dQ(i). P(i) stays
-// in the registers of the threads that computed it, so X is free for S(i+1) as soon as
-// dV(i) is issued, and the softmax threads compute P(i+1) while the tensor core runs dK(i)
-// and dQ(i); the drain of dQ(i) overlaps dV(i+1). The lse and delta of each query tile
-// are staged in shared memory ahead of use by a loader warp.
+// With dQ the MMA warp issues, per query tile i: dV(i), dP(i), S(i+1), dK(i), dQ(i). P(i)
+// stays in the registers of the threads that computed it, so X is free for S(i+1) as soon
+// as dV(i) is issued, and the softmax threads compute P(i+1) while the tensor core runs
+// dK(i) and dQ(i); the drain of dQ(i) overlaps dV(i+1). Without dQ the order is dK(i-1),
+// dP(i), dV(i), S(i+1): dP(i) runs while P(i) is computed, S(i+1) while dS(i) is. The lse
+// and delta of each query tile are staged in shared memory ahead of use by a loader warp.
+// The items (K/V tiles) come from a counter in the caller's workspace, passed from the
+// producer thread to the other roles through a two-slot ring in shared memory.
 //
-// Variants (template): kWithDQ = false leaves dq out (the K/V pass of the deterministic
+// Variants (template): kWithDQ = false leaves dq out (the K/V pass of the two-pass
 // backward); kAccum = true adds float32 dk / dv into the outputs instead of storing them
 // in the problem dtype (the per-step block backward of the unfused path).
 //
