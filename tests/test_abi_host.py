@@ -92,6 +92,20 @@ def test_workspace_size_and_check(monkeypatch):
     assert st == _abi.RA_ERR_WORKSPACE
 
 
+def test_workspace_layout():
+    """Backward workspace: the per-row dot(dout, out) in 256-byte-aligned float32, then (for
+    the tensor-core path) one 256-byte block holding the two passes' item counters; the f32
+    path needs no counters. The block backward's workspace has the same two parts."""
+    rows, hq = 2 * 64, 8
+    delta = -(-rows * hq * 4 // 256) * 256
+    p = _prob()
+    assert ra.workspace_bytes(p, 1) == delta + 256
+    assert ra.workspace_bytes(p, 2) == delta + 256
+    p32 = _prob(dtype=torch.float32, head_dim=64)
+    assert ra.workspace_bytes(p32, 1) == delta
+    assert ra.workspace_bytes(p32, 2) == delta
+
+
 @pytest.mark.parametrize("layout", W.LAYOUTS)
 @pytest.mark.parametrize("D", [1, 2, 3, 4, 8])
 def test_layout_positions_match_oracle(layout, D):
