@@ -40,13 +40,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # null until re-measured.
 TRAFFIC = {
     ("ring_bwd_tc (K/V-tile pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 55127535616 + 542334208, "source_sha": "45c9785223774eaf"},
+        {"bytes": 55050429696 + 541969408, "source_sha": "f32b290a402a8697"},
     ("ring_fwd_tc", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 180803717632 + 1260159744, "source_sha": "256c8cbfa7455492"},
+        {"bytes": 118658146816 + 1258202880, "source_sha": "2b895ee9cb12a15d"},
     ("ring_bwd_dq_tc (dq pass)", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 16182210048 + 1061005312, "source_sha": "31f2306f1323bf55"},
+        {"bytes": 16206185984 + 1060122624, "source_sha": "8733957a884564f0"},
     ("merge_kernel", "long_s131072_gqa32x8_dh128_D16_zigzag"):
-        {"bytes": 3256150528 + 2108904704, "source_sha": "416e42caefd976cc"},
+        {"bytes": 3255621888 + 2109105664, "source_sha": "59a72745c75670f4"},
 }
 
 

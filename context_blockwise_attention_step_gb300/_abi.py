@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
     P = ctypes.POINTER(RaProblem)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     sig = {
-        "ra_ring_attn_fwd": (i32, [P, vp, vp, vp, vp, vp, vp]),
+        "ra_ring_attn_fwd": (i32, [P, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]),
         "ra_block_attn_fwd": (i32, [P, i32, i32, vp, vp, vp, vp, i32, vp, vp]),
         "ra_update_out_and_lse": (i32, [P, i32, vp, vp, vp, i32, vp, vp]),
         "ra_workspace_bytes": (ctypes.c_size_t, [P, i32]),

@@ -249,11 +249,19 @@ int ra_validate(const ra_problem* p) {
 }
 
 int ra_ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const void* v, void* out,
-                     float* lse, void* stream) {
+                     float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (int e = validate(p)) return e;
   if (!q || !k || !v || !out || !lse) return fail(RA_ERR_INVALID_ARG, "null tensor pointer");
+  if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(RA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
   PlanHolder P(make_plan(p, 0, 0, p->D, -1, p->dtype == RA_F32));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // With a workspace the CTAs take their items from a counter in it; without, by stride.
+  if (workspace != nullptr && use_tc(p) && workspace_bytes >= sched_bytes(p)) {
+    P.p->work_counter = static_cast<int32_t*>(workspace);
+    const cudaError_t c = cudaMemsetAsync(workspace, 0, sizeof(int32_t), st);
+    if (c != cudaSuccess) return cuda_fail(c, "item counter clear");
+  }
   const cudaError_t e = profiled(st, [&] {
     return use_tc(p) ? ra::launch_fwd_tc(*P.p, q, k, v, out, lse, st)
                      : ra::launch_fwd_simt(*P.p, p->dtype, q, k, v, out, lse, st);
@@ -296,6 +304,7 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
 
 size_t ra_workspace_bytes(const ra_problem* p, int which) {
   if (validate(p) != RA_OK) return 0;
+  if (which == 0) return sched_bytes(p);
   if (which == 1) return delta_bytes(p) + dq_acc_bytes(p) + sched_bytes(p);
   if (which == 2) return delta_bytes(p) + sched_bytes(p);
   return 0;

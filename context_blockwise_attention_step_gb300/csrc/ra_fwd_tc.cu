@@ -67,6 +67,8 @@ struct FwdShared {
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drain;
   uint64_t xmax_bar[2][2], xl_bar[2];  // half-row exchanges: [tile][slot], [tile]
+  uint64_t item_full[2], item_empty[2];  // the CTA's item queue
+  int item[2];
   uint32_t tmem_base;
   int abort_flag;
   float xmax[2][2][2][128];  // [tile][slot][half][row]: partial row maxima
@@ -115,6 +117,30 @@ __device__ __forceinline__ void store_row32<float>(float* dst, const float (&v)[
   for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// The CTA's item queue (two slots): the producer thread takes the next item from the shared
+// counter when the caller passed a workspace (a CTA that finishes early takes more items,
+// in index order), else by the static stride, and publishes it; the MMA thread and the
+// softmax threads read it from the ring. A value >= n_items ends the walk.
+__device__ __forceinline__ int fwd_item_publish(FwdShared& sh, const Plan& P, int k,
+                                                volatile int* abort_flag, uint64_t tmo,
+                                                unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_empty[slot], ((k >> 1) & 1) ^ 1, abort_flag, tmo, status)) return -1;
+  const int w = P.work_counter ? atomicAdd(P.work_counter, 1)
+                               : static_cast<int>(blockIdx.x + static_cast<unsigned>(k) * gridDim.x);
+  sh.item[slot] = w;
+  mbar_arrive(&sh.item_full[slot]);
+  return w;
+}
+__device__ __forceinline__ int fwd_item_take(FwdShared& sh, int k, volatile int* abort_flag,
+                                             uint64_t tmo, unsigned int* status) {
+  const int slot = k & 1;
+  if (!mbar_wait(&sh.item_full[slot], (k >> 1) & 1, abort_flag, tmo, status)) return -1;
+  const int w = *reinterpret_cast<volatile int*>(&sh.item[slot]);
+  mbar_arrive(&sh.item_empty[slot]);
+  return w;
+}
+
 template <int DH, typename OutT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ring_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -150,6 +176,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(&sh.xl_bar[t], 256);
     }
     mbar_init(&sh.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.item_full[i], 1);
+      mbar_init(&sh.item_empty[i], 1 + (kFwdThreads - 128));  // MMA thread + softmax warps
+    }
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -172,7 +202,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       int kv_count = 0;
       uint32_t q_phase = 0;
-      for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+      for (int kq = 0;; ++kq) {
+        const int w = fwd_item_publish(sh, P, kq, abort_flag, tmo, status);
+        if (w < 0 || w >= P.n_items) break;
         const FwdItem it = decode_fwd(P, w);
         const FwdWalk wk = fwd_walk(P, it);
         if (wk.N == 0) continue;
@@ -221,7 +253,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t sK = smem_u32(smem + C::kOffK);
       const uint32_t sV = smem_u32(smem + C::kOffV);
       bool ok = true;
-      for (int w = blockIdx.x; w < P.n_items && ok; w += gridDim.x) {
+      for (int kq = 0; ok; ++kq) {
+        const int w = fwd_item_take(sh, kq, abort_flag, tmo, status);
+        if (w < 0) ok = false;
+        if (w < 0 || w >= P.n_items) break;
         const FwdItem it = decode_fwd(P, w);
         const FwdWalk wk = fwd_walk(P, it);
         const int N = wk.N;
@@ -302,7 +337,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint32_t s_phase = 0, od_phase = 0, xl_phase = 0;
     uint32_t xm_phase[2] = {0, 0};
     int xn = 0;  // max exchanges done (slot = xn & 1)
-    for (int w = blockIdx.x; w < P.n_items; w += gridDim.x) {
+    for (int kq = 0;; ++kq) {
+      const int w = fwd_item_take(sh, kq, abort_flag, tmo, status);
+      if (w < 0 || w >= P.n_items) break;
       const FwdItem it = decode_fwd(P, w);
       const FwdWalk wk = fwd_walk(P, it);
       if (t == 1 && !wk.two) continue;

@@ -108,8 +108,10 @@ def _check_tensor(t: torch.Tensor, dtype, numel: int, name: str):
         raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
 
 
-def ring_attn_fwd(q, k, v, prob: Problem, out=None, lse=None, stream=None):
-    """Fused ring forward -> (out, lse), shard-major. lse is float32, natural log."""
+def ring_attn_fwd(q, k, v, prob: Problem, out=None, lse=None, stream=None, workspace=None):
+    """Fused ring forward -> (out, lse), shard-major. lse is float32, natural log. The
+    workspace (``workspace_bytes(prob, 0)`` bytes; allocated when not given) holds the
+    counter the CTAs take their work items from."""
     r = prob.raw
     nq, nk = prob.rows * r.hq * r.head_dim, prob.rows * r.hkv * r.head_dim
     _check_tensor(q, prob.token_dtype, nq, "q")
@@ -119,7 +121,12 @@ def ring_attn_fwd(q, k, v, prob: Problem, out=None, lse=None, stream=None):
     lse = torch.empty(_lse_shape(prob), device=q.device, dtype=torch.float32) if lse is None else lse
     _check_tensor(out, prob.token_dtype, nq, "out")
     _check_tensor(lse, torch.float32, prob.rows * r.hq, "lse")
-    check(lib().ra_ring_attn_fwd(prob.ptr, _p(q), _p(k), _p(v), _p(out), _p(lse), _stream(stream)))
+    need = workspace_bytes(prob, 0)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(lib().ra_ring_attn_fwd(prob.ptr, _p(q), _p(k), _p(v), _p(out), _p(lse),
+                                 None if workspace is None else _p(workspace), wsz, _stream(stream)))
     return out, lse
 
 

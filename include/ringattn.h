@@ -98,9 +98,13 @@ typedef struct ra_problem {
 /* Fused ring forward: every rank r, every step s = 0..D-1 against K/V shard (r-s) mod D,
  * with the log-sum-exp merge fused (running max and denominator kept across steps).
  * q [.., Hq, Dh], k/v [.., Hkv, Dh] in the problem dtype; out like q; lse float32.
- * Needs no workspace. (nanotron how-to page, "Forward Pass Implementation".) */
+ * The workspace is optional: NULL (any workspace_bytes) runs with a static work split;
+ * a device buffer of >= ra_workspace_bytes(p, 0) bytes, 256-byte aligned, holds a counter
+ * from which the CTAs take their work items (a CTA that finishes early takes more), and is
+ * overwritten. (nanotron how-to page, "Forward Pass Implementation".) */
 int ra_ring_attn_fwd(const ra_problem* p, const void* q, const void* k, const void* v,
-                     void* out, float* lse, void* stream);
+                     void* out, float* lse, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /* One ring step of the unfused path: rank `rank` (or every rank if rank < 0) attends with
  * its query shard to the K/V shard it holds at step `step`, i.e. shard (rank-step) mod D.
@@ -122,8 +126,8 @@ int ra_update_out_and_lse(const ra_problem* p, int rank, float* out, float* lse,
                           const void* block_out, int block_out_dtype, const float* block_lse,
                           void* stream);
 
-/* Bytes of device workspace: which = 1 for ra_ring_attn_bwd, which = 2 for
- * ra_block_attn_bwd; which = 0 (forward) is 0. Returns 0 for an invalid problem as well;
+/* Bytes of device workspace: which = 0 for ra_ring_attn_fwd (optional there), which = 1
+ * for ra_ring_attn_bwd, which = 2 for ra_block_attn_bwd; 0 for which = 0 on the f32 path. Returns 0 for an invalid problem as well;
  * call ra_validate to tell the two apart. */
 size_t ra_workspace_bytes(const ra_problem* p, int which);
 

@@ -69,7 +69,7 @@ def test_validation_status(kw, status):
 
 def test_null_pointers_rejected_without_launch(built_library):
     p = _prob()
-    st = built_library.ra_ring_attn_fwd(p.ptr, None, None, None, None, None, None)
+    st = built_library.ra_ring_attn_fwd(p.ptr, None, None, None, None, None, None, 0, None)
     assert st == _abi.RA_ERR_INVALID_ARG
     st = built_library.ra_ring_attn_bwd(p.ptr, *([None] * 9), None, 0, None)
     assert st == _abi.RA_ERR_INVALID_ARG
@@ -82,7 +82,7 @@ def test_workspace_size_and_check(monkeypatch):
     rows, hq, dh = 2 * 64, 8, 128
     assert need >= rows * hq * 4  # per-row dot(dout, out)
     assert ra.workspace_bytes(p, 2) >= rows * hq * 4
-    assert ra.workspace_bytes(p, 0) == 0
+    assert ra.workspace_bytes(p, 0) == 256  # the forward's item counter (optional)
     monkeypatch.setenv("RA_BWD", "fused")  # the single-pass variant also needs float32 dq sums
     assert ra.workspace_bytes(p, 1) >= rows * hq * 4 + rows * hq * dh * 4
     monkeypatch.delenv("RA_BWD")
@@ -95,15 +95,18 @@ def test_workspace_size_and_check(monkeypatch):
 def test_workspace_layout():
     """Backward workspace: the per-row dot(dout, out) in 256-byte-aligned float32, then (for
     the tensor-core path) one 256-byte block holding the two passes' item counters; the f32
-    path needs no counters. The block backward's workspace has the same two parts."""
+    path needs no counters. The block backward's workspace has the same two parts; the
+    forward's (optional) is the counter block alone."""
     rows, hq = 2 * 64, 8
     delta = -(-rows * hq * 4 // 256) * 256
     p = _prob()
     assert ra.workspace_bytes(p, 1) == delta + 256
     assert ra.workspace_bytes(p, 2) == delta + 256
+    assert ra.workspace_bytes(p, 0) == 256
     p32 = _prob(dtype=torch.float32, head_dim=64)
     assert ra.workspace_bytes(p32, 1) == delta
     assert ra.workspace_bytes(p32, 2) == delta
+    assert ra.workspace_bytes(p32, 0) == 0
 
 
 @pytest.mark.parametrize("layout", W.LAYOUTS)
